@@ -1,0 +1,360 @@
+"""Benchmark: MLA decode (absorbed form, paged latent KV cache) on GB300.
+
+One step = one full decode call (split-KV attention kernel + LSE combine) over
+the resident synthetic MTP-3 workload (B=64, H=32, q_len=4, kv_len=81920,
+page 64, bf16 cache).  The KV stream (6.04 GB) is larger than L2, so no flush
+is needed between timed steps.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank decodes its own batch (weak scaling, no
+collective on the data path); rank 0 prints the max-over-ranks timing.
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload on this host's cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode µs/call, GB/s & % of roofline (B=64,H=32,q_len=4,kv=80k)"
+UNIT = "us/call"
+KERNEL_SRC = os.path.join(ROOT, "mla_paged_kv_02_gb300", "csrc")
+SPLIT_KERNEL_FILES = ("mla_split_kv_warp.cu", "common.cuh")
+
+
+def algorithmic_bytes(inp, out_elem_bytes):
+    """Every visible KV row read once, Q read once, out + lse written once."""
+    e = 1 if inp.kv_fp8 else 2
+    rows = inp.batch * inp.q_len * inp.num_heads
+    kv = int(inp.seq_lens.to(torch.int64).sum().item()) * 576 * e
+    return kv + rows * 576 * 2 + rows * (512 * out_elem_bytes + 4)
+
+
+def algorithmic_flops(inp):
+    """2*576 (QK) + 2*512 (PV) flops per visible (row, token) pair."""
+    L = inp.seq_lens.to(torch.int64)
+    q = inp.q_len
+    pairs = int((q * L - q * (q - 1) // 2).sum().item()) * inp.num_heads
+    return 2176 * pairs
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in SPLIT_KERNEL_FILES:
+        with open(os.path.join(KERNEL_SRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the split kernel from a committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(workload)
+    if not ent or ent.get("kernel_sha") != kernel_source_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(inp, reqs, threads=None):
+    """Time the oracle as it stands on a bounded sample (a few requests of the same
+    workload) using all host cores; scale to a whole call."""
+    import oracle
+    from mla_paged_kv_02_gb300 import synth
+
+    sub = synth.subset(inp, reqs)
+    threads = threads or os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.decode(sub, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt * inp.batch / len(reqs) * 1e6, threads, dt
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle on a bounded sample per step (rank 0 only)."""
+    if rank != 0:
+        return
+    from mla_paged_kv_02_gb300 import synth
+
+    inp = synth.make_inputs("mtp3", seed=2, device="cpu" if not torch.cuda.is_available() else "cuda")
+    reqs = [0]
+    times = []
+    for k in range(args.warmup + args.steps):
+        us, cores, dt = cpu_baseline(inp, reqs)
+        if k >= args.warmup:
+            times.append(us)
+    v = statistics.mean(times)
+    sample = f"1 of {inp.batch} requests (all {inp.num_heads * inp.q_len} rows x {int(inp.seq_lens[0])} tokens) per step, scaled x{inp.batch}"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "mtp3: B=64 H=32 q_len=4 kv_len=81920 page=64 bf16 KV, CPU oracle sample"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="mtp3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    from mla_paged_kv_02_gb300 import _lib, api, synth
+
+    _lib.load()
+    name = args.workload
+    inp = synth.make_inputs(name, seed=list(synth.WORKLOADS).index(name) + 1000 * rank, device="cuda")
+    pl = api.plan_for(inp)
+    ws = api.alloc_workspace(pl, "cuda")
+    out, lse = api.alloc_outputs(inp)
+    kvs = api.kv_scale_tensor(inp)
+    stream = torch.cuda.current_stream()
+    qn, qp = inp.q_nope.view(-1, 512), inp.q_pe.view(-1, 64)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        st = _lib.split_kv(pl, qn, qp, inp.kv_cache, inp.block_table, inp.seq_lens, inp.softmax_scale,
+                           kvs, out, lse, ws, stream)
+        if ev:
+            ev[1].record(stream)
+        st2 = _lib.combine(pl, out, lse, ws, stream)
+        if ev:
+            ev[2].record(stream)
+        assert st == 0 and st2 == 0, (st, st2)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, info = _lib.check_error(ws)
+    assert st == 0, (st, info)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    split_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    comb_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_us = total_ms / args.steps * 1e3
+    step_us = max_over_ranks(world, step_us)
+    split_us = statistics.mean(split_ms) * 1e3
+    comb_us = statistics.mean(comb_ms) * 1e3
+
+    # End to end through the public C-ABI call with host buffers: per step the
+    # per-call inputs (q_nope, q_pe, block_table, seq_lens) go host->device from
+    # pinned memory and out + lse come back; the KV cache is resident model state.
+    h_qn = qn.cpu().pin_memory()
+    h_qp = qp.cpu().pin_memory()
+    h_bt = inp.block_table.cpu().pin_memory()
+    h_sl = inp.seq_lens.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_qn, d_qp = torch.empty_like(qn), torch.empty_like(qp)
+    d_bt, d_sl = torch.empty_like(inp.block_table), torch.empty_like(inp.seq_lens)
+    h2d = sum(t.numel() * t.element_size() for t in (h_qn, h_qp, h_bt, h_sl))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        d_qn.copy_(h_qn, non_blocking=True)
+        d_qp.copy_(h_qp, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        st = _lib.decode(pl, d_qn, d_qp, inp.kv_cache, d_bt, d_sl, inp.softmax_scale, kvs, out, lse, ws, stream)
+        assert st == 0
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = max_over_ranks(world, e0.elapsed_time(e1) / args.steps * 1e3)
+    st, info = _lib.check_error(ws)
+    assert st == 0, (st, info)
+
+    hbm_peak, tc_peak, tc_sus, peak_kind = read_peaks()
+    out_b = 4 if inp.out_fp32 else 2
+    abytes = algorithmic_bytes(inp, out_b)
+    aflops = algorithmic_flops(inp)
+    achieved_gbs = abytes / (split_us * 1e-6) / 1e9
+    achieved_tf = aflops / (split_us * 1e-6) / 1e12
+    traffic = recorded_traffic(name)
+
+    line = {
+        "metric": METRIC, "value": step_us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 KV, bf16 MMA, f32 accumulate" if inp.kv_fp8 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{name}: B={inp.batch} H={inp.num_heads} q_len={inp.q_len} "
+                               f"kv_len={'x'.join(sorted(set(str(int(x)) for x in inp.seq_lens.tolist()))) if len(set(inp.seq_lens.tolist())) == 1 else 'mixed'} "
+                               f"page=64 {'e4m3' if inp.kv_fp8 else 'bf16'} KV",
+                   "num_kv_splits": pl.num_kv_splits, "chunk_tokens": pl.chunk_tokens,
+                   "row_groups": pl.row_groups, "partial_bytes": pl.partial_bytes,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "gb_per_s": abytes * world / (step_us * 1e-6) / 1e9,
+        "tflops": aflops * world / (step_us * 1e-6) / 1e12,
+        "kernel_us": {"split_kv": split_us, "combine": comb_us},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm_peak, "traffic": traffic,
+                     "peak_source": peak_kind,
+                     "tensor": {"achieved": achieved_tf, "peak": tc_peak, "unit": "TFLOP/s",
+                                "frac": achieved_tf / tc_peak}},
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (1 + (pl.num_kv_splits > 1)),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us, cores, dt = cpu_baseline(inp, [0])
+        line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"1 of {inp.batch} requests ({inp.num_heads * inp.q_len} rows x "
+                                          f"{int(inp.seq_lens[0])} tokens) in {dt:.1f} s, scaled x{inp.batch}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA paged-KV decode library.
+ *
+ * Operation (multi-head latent attention decode in absorbed form, DeepSeek-R1
+ * dims; the dims and uniform query length come from the vLLM PR #41778
+ * "TOKENSPEED_MLA" summary, risks 4 and 6; the split partial layout of width
+ * kv_lora_rank + 1 from the vLLM PR #46819 "Triton MLA attn logits
+ * preallocation" summary, key code excerpt):
+ *
+ *   Each cached token is a 576-entry row x = c_kv (512) | k_pe (64), stored in
+ *   pages of 64 tokens.  For request b with L = seq_lens[b] tokens (the q_len
+ *   new tokens included), query index i in [0, q_len) and head h:
+ *     visible V = L - q_len + 1 + i        (causal inside the q_len block)
+ *     s_t   = softmax_scale * (q_nope . c_kv_t + q_pe . k_pe_t),   t < V
+ *     out   = sum_t softmax(s)_t * c_kv_t    (512 entries)
+ *     lse   = ln sum_t exp(s_t)
+ *   With an FP8-E4M3 cache, x = e4m3 * kv_scale (one per-tensor scale).
+ *
+ * Row order everywhere: rows are (b, i, h) with flat index (b*q_len + i)*H + h.
+ *
+ * Ownership: the caller owns every buffer, including the workspace.  The
+ * library allocates no device memory, keeps no state between calls and caches
+ * no scale (a stale cached scale and a leaked per-device workspace are the two
+ * risks the TokenSpeed MLA review flags).  All device work is asynchronous on
+ * the caller's stream; no entry point but mla_decode_check_error synchronises.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,         /* a host-checkable argument is wrong            */
+    MLA_ERR_UNSUPPORTED = 2,         /* dims/page size/q_len outside what is built    */
+    MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < plan->workspace_bytes       */
+    MLA_ERR_CUDA = 4,                /* a CUDA runtime/driver call failed             */
+    MLA_ERR_DEVICE_INPUT = 5,        /* device-side check: bad seq_len or page index  */
+    MLA_ERR_TIMEOUT = 6              /* a bounded device wait gave up                 */
+} mla_status_t;
+
+typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype_t;
+typedef enum { MLA_OUT_BF16 = 0, MLA_OUT_FP32 = 1 } mla_out_dtype_t;
+
+/* Fixed geometry of the latent cache (DeepSeek-R1). */
+#define MLA_KV_LORA_RANK 512
+#define MLA_QK_ROPE_DIM 64
+#define MLA_KV_ROW (MLA_KV_LORA_RANK + MLA_QK_ROPE_DIM)
+#define MLA_PAGE_SIZE 64
+#define MLA_MAX_Q_LEN 8
+#define MLA_WORKSPACE_HEADER_BYTES 256
+
+typedef struct {
+    int batch, num_heads, q_len, max_seq_len, page_size, kv_dtype, num_sms;
+    int num_kv_splits;   /* splits per request (>= 1)                                   */
+    int chunk_tokens;    /* tokens per split, a multiple of page_size                   */
+    int rows_per_cta;    /* query rows one CTA holds                                    */
+    int row_groups;      /* ceil(num_heads * q_len / rows_per_cta)                      */
+    int reserved[3];
+    size_t partial_bytes;   /* fp32 split partials [B, q_len, H, splits, 513]; 0 if 1 split */
+    size_t workspace_bytes; /* header + partials                                        */
+} mla_decode_plan_t;
+
+/*
+ * mla_decode_plan -- host-only integer planning step (vLLM PR #46819 summary:
+ * one split-count function shared by workspace reservation and the call, so
+ * that a workspace reserved once at the worst case never has to grow).
+ *
+ *   batch, num_heads, q_len : problem shape; q_len in 1..8 (uniform per call)
+ *   max_seq_len             : an upper bound on every seq_lens[b] of the calls
+ *                             that will use this plan (>= q_len)
+ *   page_size               : must be 64
+ *   num_sms                 : SMs to plan for; 0 = query the current device
+ *   force_splits            : 0 = choose; > 0 = use this many splits (clamped
+ *                             so every split holds at least one page)
+ *   plan                    : out
+ *
+ * Splits are chosen so that batch * row_groups * splits CTAs fill whole waves
+ * of the SMs while each split keeps enough pages to amortise its set-up, and
+ * the partial bytes stay small next to the KV bytes.  Returns
+ * MLA_ERR_UNSUPPORTED for page_size != 64 or q_len outside 1..8, and
+ * MLA_ERR_INVALID_ARG for non-positive sizes.  Touches no GPU when num_sms > 0.
+ */
+mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_len, int page_size,
+                             mla_kv_dtype_t kv_dtype, int num_sms, int force_splits,
+                             mla_decode_plan_t* plan);
+
+/*
+ * mla_workspace_init -- zero the workspace header (the sticky device error
+ * word) once after the caller allocates the workspace.  Asynchronous on stream.
+ */
+mla_status_t mla_workspace_init(void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * mla_decode -- the whole decode: the split-KV attention kernel, then (when
+ * plan->num_kv_splits > 1) the LSE-weighted combine kernel.
+ *
+ *   q_nope  : bf16 rows (b,i,h), 512 used, row stride q_nope_row_stride elements
+ *   q_pe    : bf16 rows (b,i,h), 64 used, row stride q_pe_row_stride elements
+ *             (both strides multiples of 8 elements, base 16-byte aligned)
+ *   kv_cache: [num_pages, 64, 576] bf16 or e4m3 bytes (per plan->kv_dtype),
+ *             16-byte aligned, rows contiguous
+ *   block_table : int32 [batch, block_table_stride]; entries for pages
+ *             [0, ceil(L_b/64)) must lie in [0, num_pages); the rest is unread
+ *   seq_lens: int32 [batch] on the device, q_len <= L_b <= plan->max_seq_len
+ *   softmax_scale : multiplies q.x (1/sqrt(192) for DeepSeek-R1); read per call
+ *   kv_scale: device fp32 dequant scale for an FP8 cache (NULL = 1.0); read by
+ *             the kernel on every launch, never cached
+ *   out     : [batch, q_len, H, 512] bf16 or fp32 (out_dtype)
+ *   lse     : [batch, q_len, H] fp32 natural-log LSE, or NULL
+ *   workspace, workspace_bytes : >= plan->workspace_bytes, 256-byte aligned;
+ *             header zeroed once by mla_workspace_init; may be reused by any
+ *             later call whose plan needs no more bytes
+ *
+ * Host-checkable problems return at once, before any launch.  Problems only the
+ * device can see (seq_len out of range, a page index outside [0, num_pages),
+ * a wait that timed out) set the sticky error word in the workspace header and
+ * the affected request's rows are written as NaN; mla_decode_check_error
+ * reports them.  Non-uniform q_len cannot be expressed: there is no fallback.
+ */
+mla_status_t mla_decode(const mla_decode_plan_t* plan, const void* q_nope, int64_t q_nope_row_stride,
+                        const void* q_pe, int64_t q_pe_row_stride, const void* kv_cache,
+                        int num_pages, const int32_t* block_table, int block_table_stride,
+                        const int32_t* seq_lens, float softmax_scale, const float* kv_scale,
+                        void* out, mla_out_dtype_t out_dtype, float* lse, void* workspace,
+                        size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * mla_split_kv -- the first stage alone (paged KV gather, QK^T, online
+ * softmax with the causal mask, PV, split epilogue).  Same arguments as
+ * mla_decode.  With one split it writes out/lse directly; otherwise it writes
+ * the fp32 partials [B, q_len, H, splits, 513] (512 normalised outputs, then
+ * the split's LSE; an empty split writes 0 and -inf) into the workspace.
+ */
+mla_status_t mla_split_kv(const mla_decode_plan_t* plan, const void* q_nope,
+                          int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                          const void* kv_cache, int num_pages, const int32_t* block_table,
+                          int block_table_stride, const int32_t* seq_lens, float softmax_scale,
+                          const float* kv_scale, void* out, mla_out_dtype_t out_dtype, float* lse,
+                          void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * mla_combine -- the second stage alone: for every row, M = max_s lse_s,
+ * lse = M + ln sum_s exp(lse_s - M), out = sum_s exp(lse_s - lse) * o_s, read
+ * from the partials mla_split_kv wrote.  A no-op when the plan has one split.
+ */
+mla_status_t mla_combine(const mla_decode_plan_t* plan, void* out, mla_out_dtype_t out_dtype,
+                         float* lse, const void* workspace, size_t workspace_bytes,
+                         void* cuda_stream);
+
+/*
+ * mla_decode_check_error -- synchronises the stream, reads the sticky device
+ * error word from the workspace header, clears it, and returns MLA_OK,
+ * MLA_ERR_DEVICE_INPUT or MLA_ERR_TIMEOUT (or MLA_ERR_CUDA if the stream
+ * itself failed).  info (may be NULL) receives {code, request, index, value}.
+ */
+mla_status_t mla_decode_check_error(void* workspace, void* cuda_stream, int32_t info[4]);
+
+/* Human-readable name of a status code (static storage). */
+const char* mla_status_string(mla_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

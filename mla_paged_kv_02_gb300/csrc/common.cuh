@@ -1,0 +1,69 @@
+// common.cuh -- kernel parameter block and small device helpers shared by the
+// split-KV attention kernel, the combine kernel and the host launcher.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla_decode.h"
+
+namespace mla {
+
+constexpr int kKvLora = MLA_KV_LORA_RANK;  // 512: c_kv width, also the output width
+constexpr int kRope = MLA_QK_ROPE_DIM;     // 64: k_pe / q_pe width
+constexpr int kRow = MLA_KV_ROW;           // 576 entries per cached token
+constexpr int kPage = MLA_PAGE_SIZE;       // 64 tokens per page
+constexpr int kPartRow = kKvLora + 1;      // one split partial: 512 outputs + LSE
+
+// Workspace header layout (int32 words).  The first word is the sticky error
+// code (0 = none); the next three describe the first error seen.
+constexpr int kHdrCode = 0, kHdrRequest = 1, kHdrIndex = 2, kHdrValue = 3;
+
+struct DecodeParams {
+  const __nv_bfloat16* q_nope;
+  int64_t q_nope_stride;  // elements between consecutive (b,i,h) rows
+  const __nv_bfloat16* q_pe;
+  int64_t q_pe_stride;
+  const void* kv;  // [num_pages, 64, 576] bf16 or e4m3 bytes
+  int num_pages;
+  int kv_fp8;
+  const int32_t* block_table;
+  int bt_stride;
+  const int32_t* seq_lens;
+  float softmax_scale;
+  const float* kv_scale;  // device scalar or nullptr
+  void* out;              // [B*R, 512] bf16 or fp32
+  int out_fp32;
+  float* lse;       // [B*R] or nullptr
+  float* partials;  // [B*R, splits, 513] fp32 (splits > 1)
+  int32_t* err;     // workspace header
+  int batch, num_heads, q_len, rows;  // rows = num_heads * q_len per request
+  int max_seq_len, splits, chunk_tokens, rows_per_cta, row_groups;
+};
+
+// Records the first device-side error of a call sequence (sticky until read).
+__device__ __forceinline__ void report_error(int32_t* err, int code, int request, int index,
+                                             int value) {
+  if (atomicCAS(err + kHdrCode, 0, code) == 0) {
+    err[kHdrRequest] = request;
+    err[kHdrIndex] = index;
+    err[kHdrValue] = value;
+    __threadfence();
+  }
+}
+
+// Request-level validity check shared by the attention kernels: the length
+// must cover the q_len new tokens and stay within the planned maximum.
+__device__ __forceinline__ bool seq_len_ok(const DecodeParams& p, int L) {
+  return L >= p.q_len && L <= p.max_seq_len;
+}
+
+__device__ __forceinline__ void store_out(const DecodeParams& p, int64_t row, int d, float v) {
+  if (p.out_fp32)
+    reinterpret_cast<float*>(p.out)[row * kKvLora + d] = v;
+  else
+    reinterpret_cast<__nv_bfloat16*>(p.out)[row * kKvLora + d] = __float2bfloat16_rn(v);
+}
+
+}  // namespace mla

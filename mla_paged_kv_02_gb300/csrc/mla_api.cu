@@ -1,0 +1,250 @@
+// mla_api.cu -- host side of the C ABI: split planner, argument validation,
+// launches, and the sticky device error word.  Allocates nothing.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace mla;
+
+namespace {
+
+// Planner constants.  kSetupPages is the fixed cost of one CTA (Q staging, TMEM
+// allocation, pipeline fill and epilogue) expressed in page-times.
+constexpr int kRowsPerCta = 64;
+constexpr int kMaxSplits = 256;
+constexpr double kSetupPages = 2.0;
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+bool plan_ok(const mla_decode_plan_t* pl) {
+  return pl && pl->batch >= 1 && pl->num_heads >= 1 && pl->q_len >= 1 &&
+         pl->q_len <= MLA_MAX_Q_LEN && pl->page_size == MLA_PAGE_SIZE && pl->max_seq_len >= pl->q_len &&
+         pl->num_kv_splits >= 1 && pl->chunk_tokens >= MLA_PAGE_SIZE &&
+         pl->chunk_tokens % MLA_PAGE_SIZE == 0 && pl->rows_per_cta == kRowsPerCta &&
+         pl->row_groups == ceil_div((int64_t)pl->num_heads * pl->q_len, kRowsPerCta) &&
+         (pl->kv_dtype == MLA_KV_BF16 || pl->kv_dtype == MLA_KV_FP8_E4M3) &&
+         (int64_t)pl->num_kv_splits * pl->chunk_tokens >= pl->max_seq_len;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+mla_status_t fill_params(const mla_decode_plan_t* pl, const void* q_nope, int64_t q_nope_row_stride,
+                         const void* q_pe, int64_t q_pe_row_stride, const void* kv_cache,
+                         int num_pages, const int32_t* block_table, int block_table_stride,
+                         const int32_t* seq_lens, float softmax_scale, const float* kv_scale,
+                         void* out, mla_out_dtype_t out_dtype, float* lse, void* workspace,
+                         size_t workspace_bytes, DecodeParams* p) {
+  if (!plan_ok(pl)) return MLA_ERR_INVALID_ARG;
+  if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !out || !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (q_nope_row_stride < MLA_KV_LORA_RANK || q_pe_row_stride < MLA_QK_ROPE_DIM ||
+      q_nope_row_stride % 8 || q_pe_row_stride % 8)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(workspace, 256))
+    return MLA_ERR_INVALID_ARG;
+  if (num_pages < 1 || (int64_t)num_pages * MLA_PAGE_SIZE > INT32_MAX) return MLA_ERR_INVALID_ARG;
+  if (block_table_stride < ceil_div(pl->max_seq_len, MLA_PAGE_SIZE)) return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_FP32) return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < pl->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+
+  memset(p, 0, sizeof *p);
+  p->q_nope = static_cast<const __nv_bfloat16*>(q_nope);
+  p->q_nope_stride = q_nope_row_stride;
+  p->q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+  p->q_pe_stride = q_pe_row_stride;
+  p->kv = kv_cache;
+  p->num_pages = num_pages;
+  p->kv_fp8 = pl->kv_dtype == MLA_KV_FP8_E4M3;
+  p->block_table = block_table;
+  p->bt_stride = block_table_stride;
+  p->seq_lens = seq_lens;
+  p->softmax_scale = softmax_scale;
+  p->kv_scale = kv_scale;
+  p->out = out;
+  p->out_fp32 = out_dtype == MLA_OUT_FP32;
+  p->lse = lse;
+  p->err = static_cast<int32_t*>(workspace);
+  p->partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + MLA_WORKSPACE_HEADER_BYTES);
+  p->batch = pl->batch;
+  p->num_heads = pl->num_heads;
+  p->q_len = pl->q_len;
+  p->rows = pl->num_heads * pl->q_len;
+  p->max_seq_len = pl->max_seq_len;
+  p->splits = pl->num_kv_splits;
+  p->chunk_tokens = pl->chunk_tokens;
+  p->rows_per_cta = pl->rows_per_cta;
+  p->row_groups = pl->row_groups;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_len, int page_size,
+                             mla_kv_dtype_t kv_dtype, int num_sms, int force_splits,
+                             mla_decode_plan_t* plan) {
+  if (!plan) return MLA_ERR_INVALID_ARG;
+  memset(plan, 0, sizeof *plan);
+  if (batch < 1 || num_heads < 1 || q_len < 1 || max_seq_len < 1 || force_splits < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (page_size != MLA_PAGE_SIZE || q_len > MLA_MAX_Q_LEN) return MLA_ERR_UNSUPPORTED;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
+  if (max_seq_len < q_len) return MLA_ERR_INVALID_ARG;
+  if ((int64_t)num_heads * q_len > 4096) return MLA_ERR_UNSUPPORTED;
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+  }
+  const int rows = num_heads * q_len;
+  const int row_groups = ceil_div(rows, kRowsPerCta);
+  const int pages = ceil_div(max_seq_len, MLA_PAGE_SIZE);
+  const double page_bytes = (kv_dtype == MLA_KV_FP8_E4M3 ? 1.0 : 2.0) * MLA_KV_ROW * MLA_PAGE_SIZE;
+
+  int splits = 1;
+  if (force_splits > 0) {
+    splits = force_splits < pages ? force_splits : pages;
+  } else {
+    // Smallest modelled time: whole waves of one-CTA-per-SM work, each CTA paying
+    // its pages plus a fixed set-up, plus the partial write+read (and combine launch)
+    // when there is more than one split, all in per-SM page-times.
+    double best = 1e300;
+    const int smax = pages < kMaxSplits ? pages : kMaxSplits;
+    for (int s = 1; s <= smax; ++s) {
+      const int64_t ctas = (int64_t)batch * row_groups * s;
+      const int64_t waves = (ctas + num_sms - 1) / num_sms;
+      const int ppc = ceil_div(pages, s);
+      double cost = (double)waves * (ppc + kSetupPages);
+      if (s > 1) {
+        const double pbytes = 2.0 * batch * rows * (double)s * (MLA_KV_LORA_RANK + 1) * 4.0;
+        cost += pbytes / (num_sms * page_bytes) + kSetupPages;
+      }
+      if (cost < best * (1.0 - 1e-9)) {
+        best = cost;
+        splits = s;
+      }
+    }
+  }
+  const int chunk_pages = ceil_div(pages, splits);
+  splits = ceil_div(pages, chunk_pages);  // no split lies wholly past max_seq_len
+
+  plan->batch = batch;
+  plan->num_heads = num_heads;
+  plan->q_len = q_len;
+  plan->max_seq_len = max_seq_len;
+  plan->page_size = page_size;
+  plan->kv_dtype = kv_dtype;
+  plan->num_sms = num_sms;
+  plan->num_kv_splits = splits;
+  plan->chunk_tokens = chunk_pages * MLA_PAGE_SIZE;
+  plan->rows_per_cta = kRowsPerCta;
+  plan->row_groups = row_groups;
+  plan->partial_bytes =
+      splits > 1 ? (size_t)batch * rows * splits * (MLA_KV_LORA_RANK + 1) * sizeof(float) : 0;
+  plan->workspace_bytes = MLA_WORKSPACE_HEADER_BYTES + plan->partial_bytes;
+  return MLA_OK;
+}
+
+mla_status_t mla_workspace_init(void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (!workspace || workspace_bytes < MLA_WORKSPACE_HEADER_BYTES) return MLA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(workspace, 0, MLA_WORKSPACE_HEADER_BYTES, (cudaStream_t)cuda_stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+mla_status_t mla_split_kv(const mla_decode_plan_t* plan, const void* q_nope, int64_t q_nope_row_stride,
+                          const void* q_pe, int64_t q_pe_row_stride, const void* kv_cache,
+                          int num_pages, const int32_t* block_table, int block_table_stride,
+                          const int32_t* seq_lens, float softmax_scale, const float* kv_scale,
+                          void* out, mla_out_dtype_t out_dtype, float* lse, void* workspace,
+                          size_t workspace_bytes, void* cuda_stream) {
+  DecodeParams p;
+  mla_status_t st = fill_params(plan, q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache,
+                                num_pages, block_table, block_table_stride, seq_lens, softmax_scale,
+                                kv_scale, out, out_dtype, lse, workspace, workspace_bytes, &p);
+  if (st != MLA_OK) return st;
+  if (launch_split_kv(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status_t mla_combine(const mla_decode_plan_t* plan, void* out, mla_out_dtype_t out_dtype,
+                         float* lse, const void* workspace, size_t workspace_bytes,
+                         void* cuda_stream) {
+  if (!plan_ok(plan) || !out || !workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_FP32) return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (plan->num_kv_splits == 1) return MLA_OK;
+  DecodeParams p;
+  memset(&p, 0, sizeof p);
+  p.out = out;
+  p.out_fp32 = out_dtype == MLA_OUT_FP32;
+  p.lse = lse;
+  p.partials = reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(workspace)) +
+                                        MLA_WORKSPACE_HEADER_BYTES);
+  p.batch = plan->batch;
+  p.num_heads = plan->num_heads;
+  p.q_len = plan->q_len;
+  p.rows = plan->num_heads * plan->q_len;
+  p.splits = plan->num_kv_splits;
+  if (launch_combine(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status_t mla_decode(const mla_decode_plan_t* plan, const void* q_nope, int64_t q_nope_row_stride,
+                        const void* q_pe, int64_t q_pe_row_stride, const void* kv_cache,
+                        int num_pages, const int32_t* block_table, int block_table_stride,
+                        const int32_t* seq_lens, float softmax_scale, const float* kv_scale,
+                        void* out, mla_out_dtype_t out_dtype, float* lse, void* workspace,
+                        size_t workspace_bytes, void* cuda_stream) {
+  mla_status_t st = mla_split_kv(plan, q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache,
+                                 num_pages, block_table, block_table_stride, seq_lens,
+                                 softmax_scale, kv_scale, out, out_dtype, lse, workspace,
+                                 workspace_bytes, cuda_stream);
+  if (st != MLA_OK) return st;
+  return mla_combine(plan, out, out_dtype, lse, workspace, workspace_bytes, cuda_stream);
+}
+
+mla_status_t mla_decode_check_error(void* workspace, void* cuda_stream, int32_t info[4]) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)cuda_stream;
+  int32_t h[4] = {0, 0, 0, 0};
+  if (cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemcpyAsync(h, workspace, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  if (info) memcpy(info, h, sizeof h);
+  if (h[kHdrCode] != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof h, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    return h[kHdrCode] == MLA_ERR_TIMEOUT ? MLA_ERR_TIMEOUT : MLA_ERR_DEVICE_INPUT;
+  }
+  return MLA_OK;
+}
+
+const char* mla_status_string(mla_status_t status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_DEVICE_INPUT: return "MLA_ERR_DEVICE_INPUT";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// mla_combine.cu -- LSE-weighted merge of split-KV partials.
+//
+// The partial layout [rows, splits, kv_lora_rank + 1] (512 normalised outputs,
+// then the split's LSE) is the attn_logits layout of the Triton MLA split-KV
+// path (vLLM PR #46819 summary, key code excerpt).  For each row:
+//   M   = max_s lse_s
+//   lse = M + ln sum_s exp(lse_s - M)
+//   out = sum_s exp(lse_s - lse) * o_s
+// Empty splits carry lse_s = -inf and weigh zero.  One warp per row; each lane
+// owns 16 of the 512 output columns, so every load of a split's 2 KB is a fully
+// coalesced 128-byte transaction per lane group.  HBM-bound.
+#include "common.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (row >= (int64_t)p.batch * p.rows) return;
+  const float* part = p.partials + row * p.splits * kPartRow;
+
+  // Pass 1: the largest split LSE (NaN marks a request the split kernel rejected).
+  float M = -INFINITY;
+  bool nan_seen = false;
+  for (int s = lane; s < p.splits; s += 32) {
+    const float v = part[(int64_t)s * kPartRow + kKvLora];
+    nan_seen |= (v != v);
+    M = fmaxf(M, v);
+  }
+  M = warp_max(M);
+  nan_seen = __any_sync(0xffffffffu, nan_seen);
+
+  float acc = 0.f;
+  for (int s = lane; s < p.splits; s += 32) {
+    const float v = part[(int64_t)s * kPartRow + kKvLora];
+    acc += (v == -INFINITY) ? 0.f : __expf(v - M);
+  }
+  acc = warp_sum(acc);
+  const float lse = (M == -INFINITY || nan_seen) ? (nan_seen ? NAN : -INFINITY) : M + logf(acc);
+
+  float o[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) o[k] = 0.f;
+  if (!nan_seen && M != -INFINITY) {
+    for (int s = 0; s < p.splits; ++s) {
+      const float* ps = part + (int64_t)s * kPartRow;
+      const float v = ps[kKvLora];
+      if (v == -INFINITY) continue;
+      const float w = __expf(v - lse);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) o[k] = fmaf(w, ps[lane + 32 * k], o[k]);
+    }
+  } else if (nan_seen) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o[k] = NAN;
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) store_out(p, row, lane + 32 * k, o[k]);
+  if (p.lse && lane == 0) p.lse[row] = lse;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.batch * p.rows;
+  const unsigned blocks = (unsigned)((rows + kWarps - 1) / kWarps);
+  combine_kernel<<<blocks, kWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

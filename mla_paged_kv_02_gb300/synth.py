@@ -263,3 +263,28 @@ def permute_pages(inp: Inputs, seed: int) -> Inputs:
     d.kv_cache = kv
     d.block_table = bt_cpu.to(inp.block_table.device)
     return d
+
+
+def subset(inp: Inputs, reqs) -> Inputs:
+    """Host copy of the listed requests only: their pages gathered into a compact cache
+    with a remapped block table (pure data movement, for evaluating a sample)."""
+    pages, bt_rows, lens = [], [], []
+    nxt = 0
+    for b in reqs:
+        L = int(inp.seq_lens[b])
+        n = (L + inp.page_size - 1) // inp.page_size
+        pages.append(inp.block_table[b, :n].long())
+        bt_rows.append(torch.arange(nxt, nxt + n, dtype=torch.int32))
+        nxt += n
+        lens.append(L)
+    kv = inp.kv_cache[torch.cat(pages)].cpu()
+    width = max(len(r) for r in bt_rows)
+    bt = torch.full((len(reqs), width), -1, dtype=torch.int32)
+    for k, r in enumerate(bt_rows):
+        bt[k, : len(r)] = r
+    idx = torch.tensor(list(reqs), device=inp.q_nope.device)
+    return Inputs(batch=len(reqs), num_heads=inp.num_heads, q_len=inp.q_len,
+                  page_size=inp.page_size, q_nope=inp.q_nope[idx].cpu(), q_pe=inp.q_pe[idx].cpu(),
+                  kv_cache=kv, kv_fp8=inp.kv_fp8, kv_scale=inp.kv_scale, block_table=bt,
+                  seq_lens=torch.tensor(lens, dtype=torch.int32), softmax_scale=inp.softmax_scale,
+                  out_fp32=inp.out_fp32)
