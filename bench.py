@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA decode µs/call, GB/s & % of roofline (B=64,H=32,q_len=4,kv=80k)"
 UNIT = "us/call"
 KERNEL_SRC = os.path.join(ROOT, "mla_paged_kv_02_gb300", "csrc")
-SPLIT_KERNEL_FILES = ("mla_split_kv_warp.cu", "common.cuh")
+SPLIT_KERNEL_FILES = ("mla_split_kv_tc.cu", "ptx_sm100.cuh", "common.cuh")
 
 
 def algorithmic_bytes(inp, out_elem_bytes):
