@@ -211,6 +211,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="mtp3")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the request count (smaller cases of the same kernel for ncu)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -224,7 +226,8 @@ def main():
 
     _lib.load()
     name = args.workload
-    inp = synth.make_inputs(name, seed=list(synth.WORKLOADS).index(name) + 1000 * rank, device="cuda")
+    inp = synth.make_inputs(name, seed=list(synth.WORKLOADS).index(name) + 1000 * rank, device="cuda",
+                            batch=args.batch)
     pl = api.plan_for(inp)
     ws = api.alloc_workspace(pl, "cuda")
     out, lse = api.alloc_outputs(inp)

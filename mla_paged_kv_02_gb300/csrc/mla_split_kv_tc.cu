@@ -66,6 +66,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far above any legitimate wait
+constexpr int kPrefetchPages = 4;  // pages pulled into L2 ahead of the 2-stage shared-memory ring
 
 constexpr uint32_t kIdescQK = idesc_bf16(64, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true, false);
@@ -202,6 +203,18 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_pages > 0) {
       prefetch_tmap(&tm_kv);
+      // A page is one contiguous 64 x 576 block of the cache: pull the next few into
+      // L2 so that a stage, once freed, refills at L2 rather than HBM latency.
+      const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride + first_page;
+      const int64_t page_bytes = (int64_t)kPage * kRow * (kFp8 ? 1 : 2);
+      auto prefetch_page = [&](int j) {
+        if (j < n_pages) {
+          const int pg = bt_row[j];
+          if (pg >= 0 && pg < p.num_pages)
+            prefetch_l2(static_cast<const uint8_t*>(p.kv) + pg * page_bytes, (uint32_t)page_bytes);
+        }
+      };
+      for (int j = 0; j < kPrefetchPages; ++j) prefetch_page(j);
       const int qrow = b * p.rows + row0;
       mbar_arrive_expect_tx(&ctl->q_full, kChunks * kChunkBytes);
       for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * kChunkBytes, &tm_qn, &ctl->q_full, c * 64, qrow);
@@ -210,7 +223,8 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
       for (int j = 0; j < n_pages; ++j) {
         const int s = j & 1;
         if (!wait_bar(ctl, &ctl->empty[s], ((j >> 1) & 1) ^ 1, p, 1)) break;
-        const int page = p.block_table[(int64_t)b * p.bt_stride + first_page + j];
+        prefetch_page(j + kPrefetchPages);
+        const int page = bt_row[j];
         uint64_t* land = kFp8 ? &ctl->raw_full[s] : &ctl->full[s];
         if (page < 0 || page >= p.num_pages) {
           report_error(p.err, MLA_ERR_DEVICE_INPUT, b, first_page + j, page);
