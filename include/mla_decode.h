@@ -154,6 +154,34 @@ mla_status_t mla_combine(const mla_decode_plan_t* plan, void* out, mla_out_dtype
                          void* cuda_stream);
 
 /*
+ * mla_decode_noalloc -- mla_decode for callers that cannot allocate device
+ * memory (code running inside a host framework that owns every device
+ * allocation, or a plug-in handed only input/output pointers).  No counterpart
+ * exists on the source pages: it is an addition of this library.
+ *
+ * Same arguments as mla_decode without the workspace: the workspace is a
+ * fixed array of MLA_NOALLOC_SCRATCH_BYTES inside the library's device image,
+ * reserved on every GPU that loads the library until the process exits.
+ * Nothing is allocated by this call.
+ *   - plan->workspace_bytes above MLA_NOALLOC_SCRATCH_BYTES returns
+ *     MLA_ERR_WORKSPACE_TOO_SMALL before any launch (plan with fewer splits;
+ *     one split needs only the 256-byte header).
+ *   - Every call on a device shares the array and it keeps the last call's
+ *     contents; calls that may overlap on the GPU race on it, so order them.
+ *   - The first call on a device looks up and caches the array's device
+ *     address; make it before any stream capture starts.
+ *   - The error word is cleared at the start of each call; device-side input
+ *     errors show up only as NaN rows of the affected request.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+mla_status_t mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q_nope,
+                                int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                                const void* kv_cache, int num_pages, const int32_t* block_table,
+                                int block_table_stride, const int32_t* seq_lens, float softmax_scale,
+                                const float* kv_scale, void* out, mla_out_dtype_t out_dtype, float* lse,
+                                void* cuda_stream);
+
+/*
  * mla_decode_check_error -- synchronises the stream, reads the sticky device
  * error word from the workspace header, clears it, and returns MLA_OK,
  * MLA_ERR_DEVICE_INPUT or MLA_ERR_TIMEOUT (or MLA_ERR_CUDA if the stream

@@ -36,6 +36,7 @@ EXPORTED = (
     "mla_split_kv",
     "mla_combine",
     "mla_decode_check_error",
+    "mla_decode_noalloc",
     "mla_status_string",
 )
 
@@ -89,10 +90,12 @@ def load() -> ctypes.CDLL:
     lib.mla_split_kv.argtypes = decode_args
     lib.mla_combine.argtypes = [PP, P, I, P, P, SZ, P]
     lib.mla_decode_check_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+    lib.mla_decode_noalloc.argtypes = [PP, P, I64, P, I64, P, I, P, I, P, F, P, P, I, P, P]
     lib.mla_status_string.argtypes = [I]
     lib.mla_status_string.restype = ctypes.c_char_p
-    for name in EXPORTED[:-1]:
-        getattr(lib, name).restype = I
+    for name in EXPORTED:
+        if name != "mla_status_string":
+            getattr(lib, name).restype = I
     _lib = lib
     return lib
 
@@ -161,3 +164,13 @@ def check_error(workspace, stream=None):
     info = (ctypes.c_int32 * 4)()
     st = load().mla_decode_check_error(_ptr(workspace), _stream(stream), info)
     return st, list(info)
+
+
+def decode_noalloc(pl: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, softmax_scale, kv_scale,
+                   out, lse, stream=None) -> int:
+    """mla_decode_noalloc: the library's own fixed scratch array stands in for the workspace."""
+    return load().mla_decode_noalloc(
+        ctypes.byref(pl), _ptr(q_nope), q_nope.stride(-2), _ptr(q_pe), q_pe.stride(-2), _ptr(kv_cache),
+        kv_cache.shape[0], _ptr(block_table), block_table.stride(0), _ptr(seq_lens), float(softmax_scale),
+        _ptr(kv_scale), _ptr(out), MLA_OUT_FP32 if out.dtype == torch.float32 else MLA_OUT_BF16, _ptr(lse),
+        _stream(stream))
