@@ -10,9 +10,11 @@ using namespace mla;
 
 namespace {
 
-// Planner constants.  kSetupPages is the fixed cost of one CTA (Q staging, TMEM
-// allocation, pipeline fill and epilogue) expressed in page-times.
-constexpr int kRowsPerCta = 64;
+// Planner constants.  A 2-CTA cluster holds kRowsPerCta query rows (each CTA
+// half of the 576 columns).  kSetupPages is the fixed cost of one cluster (Q
+// staging, TMEM allocation, pipeline fill and epilogue) expressed in page-times.
+constexpr int kRowsPerCta = 128;
+constexpr int kCtasPerGroup = 2;
 constexpr int kMaxSplits = 256;
 constexpr double kSetupPages = 2.0;
 
@@ -118,7 +120,7 @@ mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_le
     double best = 1e300;
     const int smax = pages < kMaxSplits ? pages : kMaxSplits;
     for (int s = 1; s <= smax; ++s) {
-      const int64_t ctas = (int64_t)batch * row_groups * s;
+      const int64_t ctas = (int64_t)batch * row_groups * kCtasPerGroup * s;
       const int64_t waves = (ctas + num_sms - 1) / num_sms;
       const int ppc = ceil_div(pages, s);
       double cost = (double)waves * (ppc + kSetupPages);

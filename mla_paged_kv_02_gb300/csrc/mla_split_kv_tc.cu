@@ -1,36 +1,41 @@
 // mla_split_kv_tc.cu -- split-KV MLA decode attention on the 5th-generation
-// tensor cores (tcgen05 + TMEM) with TMA page loads, for sm_103a.
+// tensor cores (tcgen05 + TMEM), TMA page loads and a 2-CTA cluster, for sm_103a.
 //
-// One CTA = (row group of 64 query rows, split, request).  Its split covers
-// tokens [split*chunk, min((split+1)*chunk, L)) of request b; every page of it
-// is read once from HBM and shared by all 64 rows (the "one KV read per tile
-// for all heads and MTP rows" reading of the TokenSpeed MLA summary's
-// sub-linear KV scan claim, vLLM PR #41778, motivation).
+// One cluster of two CTAs = (group of 128 query rows, split, request).  Its
+// split covers tokens [split*chunk, min((split+1)*chunk, L)) of request b.  Every
+// page of the split is read from HBM once and shared by all 128 rows (the
+// "one KV read per tile for all heads and MTP rows" reading of the TokenSpeed
+// MLA summary's sub-linear KV scan claim, vLLM PR #41778, motivation).
 //
-// Warp roles (192 threads):
-//   warp 0  TMA producer: Q once (9 boxes of 64 rows x 64 cols), then per page a
-//           block_table lookup and 9 boxes of 64 tokens x 64 cols (128B swizzle)
-//           into a 2-stage ring; owns the TMEM allocation.
-//   warp 1  MMA issuer (one thread):
-//             QK^T : S[64 rows x 64 tok] (TMEM) = Q[64 x 576] . K[64 x 576]^T,
-//                    tcgen05 kind::f16 M=64 N=64, 36 K-steps, both K-major.
-//             PV   : O^T[512 dims x 64 rows] (TMEM) += V^T . P^T, four M=128
-//                    dim blocks, N=64, 4 K-steps; V^T is the page's first 512
-//                    columns read MN-major, P is K-major.
-//   warps 6-9  (FP8 cache only) converter warpgroup: the page arrives as e4m3
-//           bytes in the upper half of the stage; every thread first pulls its
-//           share into registers, then the group writes exact bf16 values (e4m3 is
-//           a subset of bf16) in the 128B-swizzled layout the MMAs read.  The
-//           per-tensor scale is folded into the softmax scale and the epilogue.
-//   warps 2-5  softmax / correction / epilogue warpgroup.  Lanes 0-15 of each
-//           warp own one query row each (the M=64 accumulator places row r in
-//           TMEM lane 32*(r/16) + r%16).  Online softmax in the exp2 domain with
-//           a lazily updated reference max (rescale O only when a row's max
-//           grows by more than 2^8), causal mask, zeroing of V rows past L,
-//           P (bf16) written into the page's dead k_pe chunk, epilogue O/l.
+// The 576-wide contraction is split between the two CTAs: CTA 0 holds columns
+// [0, 256) of Q and of every page, CTA 1 holds [256, 576) (the rest of c_kv and
+// k_pe).  That keeps both operands of every MMA at 128 rows:
+//   QK^T : S_c[128 rows x 64 tok] = Q[:, cols_c] . K[:, cols_c]^T  (M=128, N=64)
+//   PV   : O_c[128 rows x 256]   += P[128 x 64] . V[64 x cols_c(256)] (M=128, N=256)
+// where each CTA's 256 V columns are exactly the first four 64-column chunks it
+// already holds.  The two partial S_c are summed across the pair through
+// distributed shared memory: CTA c owns the softmax of 64 rows (CTA 0 rows 0-63,
+// CTA 1 rows 64-127), receives the peer's partial for those rows, computes P,
+// and writes its P rows into both CTAs' P buffers.
 //
-// Shared memory (1 CTA / SM): Q 72 KB + 2 x 72 KB page stages + barriers.
-// TMEM: S double buffer at columns [0,128), O^T at [128, 384).
+// Warp roles (192 threads; 320 for an FP8 cache):
+//   warp 0     TMA producer: Q once, then per page a block-table lookup and the
+//              CTA's 4 or 5 64x64 boxes (128B swizzle) into a 2-stage ring; L2
+//              prefetch of upcoming pages; owns the TMEM allocation.
+//   warp 1     MMA issuer (one thread).
+//   warps 2-5  softmax / exchange / epilogue warpgroup.  Warp w reads TMEM lane
+//              quadrant w%4 (rows 32*(w%4) .. +31).  Quadrants of rows this CTA
+//              owns compute the softmax; the other two send their S partial rows
+//              to the peer.  Online softmax in the exp2 domain with a lazily
+//              updated reference max: O is rescaled only when a row's max grows
+//              by more than 2^8, coordinated across the pair by a per-page flag.
+//   warps 6-9  (FP8 cache) converter: the CTA's e4m3 columns land in the upper
+//              half of a stage; every thread first pulls its share into
+//              registers, then writes exact bf16 values (e4m3 is a subset of
+//              bf16) in the swizzled layout.  The per-tensor scale is folded into
+//              the softmax scale and the epilogue.
+//
+// TMEM: S double buffer at columns [0,128), O_c at [128, 384).
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -43,51 +48,64 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kRows = 64;                       // query rows per CTA
-constexpr int kChunks = 9;                      // 64-column chunks in a 576-wide row
-constexpr int kChunkBytes = 64 * 128;           // 64 rows x 128 B
-constexpr int kStageBytes = kChunks * kChunkBytes;  // one page of bf16 rows: 72 KB
+constexpr int kRows = 128;              // query rows per cluster
+constexpr int kMaxCh = 5;               // 64-column chunks a CTA holds (CTA 0: 4, CTA 1: 5)
+constexpr int kQChunkBytes = 128 * 128;  // 128 rows x 128 B
+constexpr int kKvChunkBytes = 64 * 128;  // 64 tokens x 128 B
+constexpr int kStageBytes = kMaxCh * kKvChunkBytes;
 constexpr int kStages = 2;
+constexpr int kSinBytes = 64 * 64 * 4;  // peer's partial S for the 64 owned rows
+constexpr int kPBytes = kRows * 128;    // P[128 rows x 64 tokens] bf16
 constexpr int kQOff = 0;
-constexpr int kStageOff = kQOff + kChunks * kChunkBytes;
-constexpr int kCtlOff = kStageOff + kStages * kStageBytes;
-constexpr int kSmemBytes = kCtlOff + 2048 + 1024;  // control block + 1 KB alignment slack
+constexpr int kStageOff = kQOff + kMaxCh * kQChunkBytes;
+constexpr int kSinOff = kStageOff + kStages * kStageBytes;
+constexpr int kPOff = kSinOff + 2 * kSinBytes;
+constexpr int kCtlOff = kPOff + 2 * kPBytes;
+constexpr int kCtlBytes = 2048;
+constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kPOff % 1024 == 0 && kStageOff % 1024 == 0, "swizzle atoms");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;     // two 64-column S buffers
-constexpr uint32_t kColO = 128;   // four 64-column O^T blocks (dims 128b .. 128b+127)
+constexpr uint32_t kColS = 0;    // two 64-column S buffers
+constexpr uint32_t kColO = 128;  // O_c: 256 columns
 
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kConvWarp0 = 6;
-constexpr int kRawOff = kStageBytes / 2;        // e4m3 page (36 KB) in the upper half of a stage
-constexpr int kRawBox = 64 * 64;                // one 64 tokens x 64 bytes box
+constexpr int kRawOff = kStageBytes / 2;  // e4m3 columns of a page in the upper half of a stage
+constexpr int kRawBox = 64 * 64;          // one 64 tokens x 64 bytes box
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;       // log2 units
+constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far above any legitimate wait
-constexpr int kPrefetchPages = 4;  // pages pulled into L2 ahead of the 2-stage shared-memory ring
+constexpr int kPrefetchPages = 4;
 
-constexpr uint32_t kIdescQK = idesc_bf16(64, 64, false, false);
-constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true, false);
+constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
 
 struct Ctl {
   uint64_t q_full;
-  uint64_t raw_full[kStages];  // FP8: e4m3 bytes landed
+  uint64_t raw_full[kStages];
   uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t s_full[kStages];
-  uint64_t s_free[kStages];
-  uint64_t p_full[kStages];
+  uint64_t empty[kStages];     // this CTA's PV of the stage's page has completed
+  uint64_t s_full[kStages];    // QK^T of the page is in TMEM
+  uint64_t s_free[kStages];    // the 4 softmax warps have read it (count 4)
+  uint64_t sin_full[2];        // peer's 2 sender warps delivered partial S (count 2, remote)
+  uint64_t sin_free[2];        // peer's 2 owner warps consumed what this CTA sent (count 2, remote)
+  uint64_t p_free[2];          // PV of the buffer's previous page done in both CTAs (count 2)
+  uint64_t pv_ready[2];        // both CTAs' owners wrote P (count 4: 2 local + 2 remote)
+  uint64_t rescaled[2];        // the 4 local warps rescaled O (count 4)
+  uint64_t fin;                // 1/l of all 128 rows delivered (count 4)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int poisoned;
-  float fac[kRows];
+  int flag[2];                 // page+1 when some row of that page needs O rescaled
+  float fac[2][kRows];
   float inv_l[kRows];
-  float lse[kRows];
 };
-static_assert(sizeof(Ctl) <= 2048, "control block");
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -100,8 +118,9 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// Named barrier over the softmax warpgroup (barrier 1, 128 threads), with an OR
-// reduction of a predicate.
+// Named barrier over the softmax warpgroup (barrier 1, 128 threads), OR-reducing
+// a predicate.  Every decision that follows a bounded wait goes through it, so
+// no thread can reach a later barrier that another thread has already left.
 __device__ __forceinline__ bool wg_sync_or(bool v) {
   uint32_t r;
   asm volatile(
@@ -130,16 +149,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
-// Bounded wait that also gives up when another role has aborted.
+// Bounded wait (acquire at cluster scope) that also gives up once any role of
+// this CTA has aborted.
 __device__ __forceinline__ bool wait_bar(Ctl* c, uint64_t* bar, uint32_t parity, const DecodeParams& p,
                                          int where) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_try_wait_cluster(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int k = 0; k < 32; ++k)
-      if (mbar_try_wait(a, parity)) return true;
+      if (mbar_try_wait_cluster(a, parity)) return true;
     if (*(volatile int*)&c->abort) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *(volatile int*)&c->abort = 1;
@@ -150,7 +170,7 @@ __device__ __forceinline__ bool wait_bar(Ctl* c, uint64_t* bar, uint32_t parity,
 }
 
 template <bool kFp8>
-__global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
     split_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
                        const __grid_constant__ CUtensorMap tm_kv, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -158,12 +178,18 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
   uint8_t* sQ = smem + kQOff;
   uint8_t* sKV = smem + kStageOff;
+  uint8_t* sSin = smem + kSinOff;
+  uint8_t* sP = smem + kPOff;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rg = blockIdx.x;     // row group
-  const int split = blockIdx.y;  // split index
-  const int b = blockIdx.z;      // request
+  const uint32_t cta = cluster_ctarank();  // 0 or 1: which column half this CTA holds
+  const uint32_t peer = cta ^ 1u;
+  const int nch = cta == 0 ? 4 : 5;        // 64-column chunks held
+  const int g0 = cta == 0 ? 0 : 4;         // first global chunk
+  const int rg = blockIdx.x >> 1;          // row group
+  const int split = blockIdx.y;
+  const int b = blockIdx.z;
 
   const int L = p.seq_lens[b];
   const bool len_ok = seq_len_ok(p, L);
@@ -171,8 +197,9 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
   const int hi = len_ok ? min(lo + p.chunk_tokens, L) : lo;
   const int first_page = lo / kPage;
   const int n_pages = hi > lo ? (hi + kPage - 1) / kPage - first_page : 0;
-  const int row0 = rg * kRows;  // first row of this group within the request
+  const int row0 = rg * kRows;
   const float kv_scale = (kFp8 && p.kv_scale) ? *p.kv_scale : 1.0f;
+  const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride + first_page;
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
@@ -182,13 +209,21 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
       mbar_init(&ctl->empty[s], 1);
       mbar_init(&ctl->s_full[s], 1);
       mbar_init(&ctl->s_free[s], 4);
-      mbar_init(&ctl->p_full[s], 4);
     }
+    for (int e = 0; e < 2; ++e) {
+      mbar_init(&ctl->sin_full[e], 2);
+      mbar_init(&ctl->sin_free[e], 2);
+      mbar_init(&ctl->p_free[e], 2);
+      mbar_init(&ctl->pv_ready[e], 4);
+      mbar_init(&ctl->rescaled[e], 4);
+      ctl->flag[e] = 0;
+    }
+    mbar_init(&ctl->fin, 4);
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
     ctl->poisoned = len_ok ? 0 : 1;
     fence_mbarrier_init();
-    if (!len_ok && split == 0 && rg == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, -1, L);
+    if (!len_ok && split == 0 && rg == 0 && cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, -1, L);
   }
   if (warp == 0) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -196,6 +231,7 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
@@ -203,12 +239,11 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_pages > 0) {
       prefetch_tmap(&tm_kv);
-      // A page is one contiguous 64 x 576 block of the cache: pull the next few into
-      // L2 so that a stage, once freed, refills at L2 rather than HBM latency.
-      const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride + first_page;
       const int64_t page_bytes = (int64_t)kPage * kRow * (kFp8 ? 1 : 2);
+      // A page is one contiguous block of the cache; CTA 0 pulls the next few
+      // whole pages into L2 so that freed stages refill at L2 latency.
       auto prefetch_page = [&](int j) {
-        if (j < n_pages) {
+        if (cta == 0 && j < n_pages) {
           const int pg = bt_row[j];
           if (pg >= 0 && pg < p.num_pages)
             prefetch_l2(static_cast<const uint8_t*>(p.kv) + pg * page_bytes, (uint32_t)page_bytes);
@@ -216,31 +251,39 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
       };
       for (int j = 0; j < kPrefetchPages; ++j) prefetch_page(j);
       const int qrow = b * p.rows + row0;
-      mbar_arrive_expect_tx(&ctl->q_full, kChunks * kChunkBytes);
-      for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * kChunkBytes, &tm_qn, &ctl->q_full, c * 64, qrow);
-      tma_load_2d(sQ + 8 * kChunkBytes, &tm_qp, &ctl->q_full, 0, qrow);
+      mbar_arrive_expect_tx(&ctl->q_full, nch * kQChunkBytes);
+      for (int k = 0; k < nch; ++k) {
+        const int g = g0 + k;
+        if (g < 8)
+          tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, g * 64, qrow);
+        else
+          tma_load_2d(sQ + k * kQChunkBytes, &tm_qp, &ctl->q_full, 0, qrow);
+      }
       int issued = 0;
+      int next_page = bt_row[0];
       for (int j = 0; j < n_pages; ++j) {
         const int s = j & 1;
+        const int page = next_page;
+        if (j + 1 < n_pages) next_page = bt_row[j + 1];  // lookup ahead of the wait
         if (!wait_bar(ctl, &ctl->empty[s], ((j >> 1) & 1) ^ 1, p, 1)) break;
         prefetch_page(j + kPrefetchPages);
-        const int page = bt_row[j];
         uint64_t* land = kFp8 ? &ctl->raw_full[s] : &ctl->full[s];
+        uint8_t* stage = sKV + s * kStageBytes;
         if (page < 0 || page >= p.num_pages) {
-          report_error(p.err, MLA_ERR_DEVICE_INPUT, b, first_page + j, page);
+          if (cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, first_page + j, page);
           mbar_arrive(land);  // nothing to load; consumers mask the whole page
         } else if (kFp8) {
-          mbar_arrive_expect_tx(land, kChunks * kRawBox);
-          uint8_t* dst = sKV + s * kStageBytes + kRawOff;
-          for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kRawBox, &tm_kv, land, c * 64, page * kPage);
+          mbar_arrive_expect_tx(land, nch * kRawBox);
+          for (int k = 0; k < nch; ++k)
+            tma_load_2d(stage + kRawOff + k * kRawBox, &tm_kv, land, (g0 + k) * 64, page * kPage);
         } else {
-          mbar_arrive_expect_tx(land, kStageBytes);
-          uint8_t* dst = sKV + s * kStageBytes;
-          for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, &tm_kv, land, c * 64, page * kPage);
+          mbar_arrive_expect_tx(land, nch * kKvChunkBytes);
+          for (int k = 0; k < nch; ++k)
+            tma_load_2d(stage + k * kKvChunkBytes, &tm_kv, land, (g0 + k) * 64, page * kPage);
         }
         issued = j + 1;
       }
-      // Never leave with copies in flight: wait (bounded) for the last stages to land.
+      // Never leave with copies in flight.
       for (int j = max(0, issued - kStages); j < issued; ++j) {
         uint64_t* land = kFp8 ? &ctl->raw_full[j & 1] : &ctl->full[j & 1];
         const uint64_t t0 = globaltimer_ns();
@@ -251,26 +294,27 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_pages > 0) {
-      const uint32_t q_addr = smem_u32(sQ);
+      const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint32_t kv_addr = smem_u32(sKV);
-      const uint64_t q_desc = sdesc_sw128(q_addr, 16, 1024);
+      const uint32_t p_addr = smem_u32(sP);
+      int nres[2] = {0, 0};
       bool ok = wait_bar(ctl, &ctl->q_full, 0, p, 2);
-      int pv_issued = 0;
       auto issue_pv = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!wait_bar(ctl, &ctl->p_full[s], (j >> 1) & 1, p, 5)) return false;
+        const int e = j & 1;
+        if (!wait_bar(ctl, &ctl->pv_ready[e], (j >> 1) & 1, p, 5)) return false;
+        if (*(volatile int*)&ctl->flag[e] == j + 1) {  // some row's reference max moved
+          if (!wait_bar(ctl, &ctl->rescaled[e], nres[e] & 1, p, 10)) return false;
+          ++nres[e];
+        }
         tc_fence_after();
-        const uint32_t st = kv_addr + s * kStageBytes;
-        const uint64_t v_desc = sdesc_sw128(st, 8192, 1024);
-        const uint64_t p_desc = sdesc_sw128(st + 8 * kChunkBytes, 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(kv_addr + e * kStageBytes, kKvChunkBytes, 1024);
+        const uint64_t p_desc = sdesc_sw128(p_addr + e * kPBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-          for (int blk = 0; blk < 4; ++blk)
-            mma_bf16_ss(tmem + kColO + blk * 64, v_desc + (uint64_t)((blk * 2 * kChunkBytes + kk * 2048) >> 4),
-                        p_desc + (uint64_t)((kk * 32) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&ctl->empty[s]);  // frees the stage and marks O^T current through page j
-        ++pv_issued;
+          mma_bf16_ss(tmem + kColO, p_desc + (uint64_t)((kk * 32) >> 4), v_desc + (uint64_t)((kk * 2048) >> 4),
+                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&ctl->empty[e]);               // stage free; O current through page j
+        mma_commit_multicast(&ctl->p_free[e], 3);  // P buffer e reusable, in both CTAs
         return true;
       };
       for (int j = 0; ok && j < n_pages; ++j) {
@@ -280,53 +324,48 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
         tc_fence_after();
         const uint64_t k_desc = sdesc_sw128(kv_addr + s * kStageBytes, 16, 1024);
         const uint32_t d = tmem + kColS + s * 64;
+        for (int k = 0; k < nch; ++k) {
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16_ss(d, q_desc + (uint64_t)((c * kChunkBytes + k * 32) >> 4),
-                        k_desc + (uint64_t)((c * kChunkBytes + k * 32) >> 4), kIdescQK, (c | k) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d, q_desc + (uint64_t)((k * kQChunkBytes + kk * 32) >> 4),
+                        k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4), kIdescQK, (k | kk) ? 1u : 0u);
+        }
         mma_commit(&ctl->s_full[s]);
         if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok) issue_pv(n_pages - 1);
-      // Drain: every MMA this thread issued has completed before TMEM is freed.
-      mma_commit(&ctl->drain);
+      mma_commit(&ctl->drain);  // every MMA of this thread has completed before TMEM is freed
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(smem_u32(&ctl->drain), 0))
         if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-      (void)pv_issued;
     }
   } else if (kFp8 && warp >= kConvWarp0) {
     // ------------------------------------------------------------ e4m3 -> bf16 converter
     const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
+    const int units = nch * 64;                    // (chunk, token) pairs of 64 bytes
     for (int j = 0; j < n_pages; ++j) {
       const int s = j & 1;
-      // Every decision after a bounded wait is made uniform across the group, so no
-      // thread can reach a named barrier that another thread has already left.
       if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[s], (j >> 1) & 1, p, 9))) break;
       uint8_t* stage = sKV + s * kStageBytes;
-      // Unit u = (chunk c, token t): 64 e4m3 bytes at raw box c, row t.  Pull all
-      // of this thread's units into registers before anyone overwrites the raw half.
-      uint4 raw[5][4];
+      uint4 raw[3][4];
 #pragma unroll
-      for (int k = 0; k < 5; ++k) {
+      for (int k = 0; k < 3; ++k) {
         const int u = ct + k * 128;
-        if (u < kChunks * 64) {
+        if (u < units) {
           const uint4* src = reinterpret_cast<const uint4*>(stage + kRawOff + (u >> 6) * kRawBox + (u & 63) * 64);
 #pragma unroll
           for (int q = 0; q < 4; ++q) raw[k][q] = src[q];
         }
       }
-      conv_sync();
+      conv_sync();  // every raw byte is in registers before the bf16 writes overlap them
 #pragma unroll
-      for (int k = 0; k < 5; ++k) {
+      for (int k = 0; k < 3; ++k) {
         const int u = ct + k * 128;
-        if (u < kChunks * 64) {
+        if (u < units) {
           const int c = u >> 6, t = u & 63;
-          uint8_t* dst = stage + c * kChunkBytes + t * 128;
+          uint8_t* dst = stage + c * kKvChunkBytes + t * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {  // 16 bytes in -> 32 bytes (two swizzled 16-byte units) out
+          for (int q = 0; q < 4; ++q) {
             const uint32_t w[4] = {raw[k][q].x, raw[k][q].y, raw[k][q].z, raw[k][q].w};
             uint32_t o[8];
 #pragma unroll
@@ -334,196 +373,270 @@ __global__ void __launch_bounds__(kFp8 ? 320 : 192, 1)
               o[2 * h] = e4m3x2_to_bf16x2((uint16_t)(w[h] & 0xFFFFu));
               o[2 * h + 1] = e4m3x2_to_bf16x2((uint16_t)(w[h] >> 16));
             }
-            const int u0 = 2 * q, u1 = 2 * q + 1;
-            *reinterpret_cast<uint4*>(dst + ((u0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(dst + ((u1 ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<uint4*>(dst + (((2 * q) ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
           }
         }
       }
       fence_proxy_async_smem();
-      conv_sync();  // the raw half of this stage is dead for every thread before the next load
+      conv_sync();
       if (lane == 0) mbar_arrive(&ctl->full[s]);
     }
-  } else {
-    // ------------------------------------------------------------ softmax warpgroup
-    const int wg_t = threadIdx.x - kSoftmaxWarp0 * 32;  // 0..127
-    const int quad = warp & 3;                          // TMEM lane quadrant this warp may access
-    const int r = quad * 16 + lane;                     // query row within the group (lanes 0-15)
-    const bool row_thread = lane < 16 && row0 + r < p.rows;
-    const int grow_local = row0 + r;                    // row within the request
-    const int qi = grow_local / p.num_heads;            // query index i of this row
-    const int vis = L - p.q_len + 1 + qi;               // visible tokens for this row
+  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+    // ------------------------------------------------------------ softmax / exchange warpgroup
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;              // row within the group (TMEM lane)
+    const bool owner = (quad >> 1) == (int)cta;  // CTA 0 owns rows 0-63, CTA 1 rows 64-127
+    const int ri = r & 63;                       // row index within the owned / sent half
+    const bool row_ok = row0 + r < p.rows;
+    const int qi = (row0 + r) / p.num_heads;
+    const int vis = L - p.q_len + 1 + qi;        // tokens this row may see
     const float sc2 = p.softmax_scale * kv_scale * kLog2e;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t sin_local = smem_u32(sSin);
+    const uint32_t sin_peer = mapa_shared(sin_local, peer);
+    const uint32_t p_local = smem_u32(sP);
+    const uint32_t p_peer = mapa_shared(p_local, peer);
     float m_ref = -INFINITY, l_sum = 0.f;
     bool poisoned = !len_ok;
     bool ok = true;
+    int nres[2] = {0, 0};
+
+    // Rescale check for page jj, run one page later so senders never wait on it:
+    // if any row of either CTA moved its reference max on page jj, every warp
+    // rescales its lanes of O (rows) by fac before PV(jj) is issued.
+    auto rescale_check = [&](int jj) -> bool {
+      const int e = jj & 1;
+      bool fail = !wait_bar(ctl, &ctl->pv_ready[e], (jj >> 1) & 1, p, 11);
+      if (wg_sync_or(fail)) return false;
+      const bool resc = wg_sync_or(*(volatile int*)&ctl->flag[e] == jj + 1);
+      if (!resc) return true;
+      // O holds pages < jj once PV(jj-1) has completed (its commit covers all before).
+      fail = jj > 0 && !wait_bar(ctl, &ctl->empty[(jj - 1) & 1], ((jj - 1) >> 1) & 1, p, 12);
+      if (wg_sync_or(fail)) return false;
+      tc_fence_after();
+      __syncwarp();
+      const float f = ctl->fac[e][r];
+#pragma unroll 1
+      for (int g = 0; g < 16; ++g) {
+        uint32_t v[16];
+        const uint32_t ta = tmem + lane_base + kColO + g * 16;
+        tmem_ld16(ta, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
+        tmem_st16(ta, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->rescaled[e]);
+      ++nres[e];
+      return true;
+    };
 
     for (int j = 0; j < n_pages; ++j) {
       const int s = j & 1;
-      const int tok0 = lo + j * kPage;  // first token of page j (lo is page aligned)
-      const int page = p.block_table[(int64_t)b * p.bt_stride + first_page + j];
+      const int tok0 = lo + j * kPage;  // lo is page aligned
+      const int page = bt_row[j];
       const bool page_ok = page >= 0 && page < p.num_pages;
       poisoned |= !page_ok;
-      // Uniform across the warpgroup (see the converter): a late arrival cannot split it.
       if (wg_sync_or(!wait_bar(ctl, &ctl->s_full[s], (j >> 1) & 1, p, 6))) { ok = false; break; }
       tc_fence_after();
       __syncwarp();
       float sv[64];
       {
-        uint32_t raw[16];
+        uint32_t raw[4][16];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          tmem_ld16(tmem + lane_base + kColS + s * 64 + g * 16, raw);
-          tmem_ld_wait();
+        for (int g = 0; g < 4; ++g) tmem_ld16(tmem + lane_base + kColS + s * 64 + g * 16, raw[g]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 16; ++k) sv[g * 16 + k] = __uint_as_float(raw[k]);
-        }
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) sv[g * 16 + k] = __uint_as_float(raw[g][k]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->s_free[s]);
 
-      // Mask and scale: token tok0+c is visible to this row iff tok0+c < vis.
-      const int n_vis = page_ok ? min(max(vis - tok0, 0), kPage) : 0;
-      float mx = -INFINITY;
+      bool fail = false;
+      if (!owner) {
+        // ---- sender: partial S of a row the peer owns -> peer's S_in[e][ri]
+        if (wait_bar(ctl, &ctl->sin_free[s], ((j >> 1) & 1) ^ 1, p, 13)) {
+          const uint32_t dst = sin_peer + s * kSinBytes + ri * 256;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float x = (row_thread && c < n_vis) ? sv[c] * sc2 : -INFINITY;
-        sv[c] = x;
-        mx = fmaxf(mx, x);
-      }
-      const bool need = row_thread && (mx > m_ref + kRescaleThreshold);
-      if (wg_sync_or(need)) {
-        float fac = 1.f;
-        if (need) {
-          fac = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
-          l_sum *= fac;
-          m_ref = mx;
+          for (int u = 0; u < 16; ++u)
+            st_cluster_v4(dst + ((u ^ (ri & 7)) << 4),
+                          make_uint4(__float_as_uint(sv[4 * u]), __float_as_uint(sv[4 * u + 1]),
+                                     __float_as_uint(sv[4 * u + 2]), __float_as_uint(sv[4 * u + 3])));
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->sin_full[s]), peer));
+        } else {
+          fail = true;
         }
-        if (lane < 16) ctl->fac[r] = fac;
-        // O^T holds pages < j once PV(j-1) has completed (its commit also covers
-        // every earlier MMA); only then may its columns be rescaled.
-        bool fail = j > 0 && !wait_bar(ctl, &ctl->empty[(j - 1) & 1], ((j - 1) >> 1) & 1, p, 7);
-        fail = wg_sync_or(fail);  // uniform decision; also publishes fac[]
-        tc_fence_after();
-        if (fail) { ok = false; break; }
-        __syncwarp();
-        if (j > 0) {
-#pragma unroll 1
-          for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
-              uint32_t v[16];
-              const uint32_t ta = tmem + lane_base + kColO + blk * 64 + g * 16;
-              tmem_ld16(ta, v);
-              tmem_ld_wait();
+      } else {
+        // ---- owner: add the peer's partial, softmax, P into both CTAs
+        if (wait_bar(ctl, &ctl->sin_full[s], (j >> 1) & 1, p, 14)) {
+          const float4* src = reinterpret_cast<const float4*>(sSin + s * kSinBytes + ri * 256);
 #pragma unroll
-              for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * ctl->fac[g * 16 + k]);
-              tmem_st16(ta, v);
+          for (int u = 0; u < 16; ++u) {
+            const float4 v = src[u ^ (ri & 7)];
+            sv[4 * u] += v.x;
+            sv[4 * u + 1] += v.y;
+            sv[4 * u + 2] += v.z;
+            sv[4 * u + 3] += v.w;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->sin_free[s]), peer));
+
+          // V rows of tokens at or past L (or of a page that was never loaded) may
+          // hold anything, NaN included; zero this CTA's 256 V columns of them.
+          const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
+          if (ri >= n_valid) {
+            uint8_t* stage = sKV + s * kStageBytes;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint4* rowp = reinterpret_cast<uint4*>(stage + c * kKvChunkBytes + ri * 128);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) rowp[u] = make_uint4(0, 0, 0, 0);
             }
           }
-          tmem_st_wait();
-        }
-        tc_fence_before();
-      }
 
-      // P = 2^(x - m_ref) as bf16 into the page's k_pe chunk (dead after QK^T),
-      // row r, 128B-swizzled K-major: 16-byte unit u of row r sits at u ^ (r & 7).
-      uint8_t* stage = sKV + s * kStageBytes;
-      if (row_thread) {
-        uint8_t* prow = stage + 8 * kChunkBytes + r * 128;
-        float part = 0.f;
+          const int n_vis = page_ok ? min(max(vis - tok0, 0), kPage) : 0;
+          float mx = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint32_t w[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
-            const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - m_ref);
-            const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - m_ref);
-            part += p0 + p1;
-            __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-            w[h] = *reinterpret_cast<uint32_t*>(&pk);
+          for (int c = 0; c < 64; ++c) {
+            const float x = (row_ok && c < n_vis) ? sv[c] * sc2 : -INFINITY;
+            sv[c] = x;
+            mx = fmaxf(mx, x);
           }
-          *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        l_sum += part;
-      }
-      // V rows of tokens at or past L (or of a page that was never loaded) may hold
-      // anything, NaN included; zero their 512 c_kv columns so 0 * V stays 0.
-      const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
-      if (n_valid < kPage) {
-        const int t = wg_t & 63;
-        if (t >= n_valid) {
-          const int c0 = (wg_t >> 6) * 4;
-#pragma unroll
-          for (int c = c0; c < c0 + 4; ++c) {
-            uint4* rowp = reinterpret_cast<uint4*>(stage + c * kChunkBytes + t * 128);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) rowp[u] = make_uint4(0, 0, 0, 0);
+          const bool need = row_ok && (mx > m_ref + kRescaleThreshold);
+          float fac = 1.f;
+          if (need) {
+            fac = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
+            l_sum *= fac;
+            m_ref = mx;
           }
+          uint4 pk[8];
+          float part = 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
+              const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - m_ref);
+              const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - m_ref);
+              part += p0 + p1;
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              w[h] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          l_sum += part;
+          // Both CTAs' PV of page j-2 must be done before P buffer s is rewritten.
+          if (wait_bar(ctl, &ctl->p_free[s], ((j >> 1) & 1) ^ 1, p, 15)) {
+            const uint32_t off = s * kPBytes + r * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint32_t o = off + ((u ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4*>(sP + o) = pk[u];
+              st_cluster_v4(p_peer + o, pk[u]);
+            }
+            ctl->fac[s][r] = fac;
+            st_cluster_u32(mapa_shared(smem_u32(&ctl->fac[s][r]), peer), __float_as_uint(fac));
+            if (need && j > 0) {  // page 0's PV overwrites O, so it never needs a rescale
+              ctl->flag[s] = j + 1;
+              st_cluster_u32(mapa_shared(smem_u32(&ctl->flag[s]), peer), (uint32_t)(j + 1));
+            }
+            fence_proxy_async_cluster();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->pv_ready[s]), cta));
+              mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->pv_ready[s]), peer));
+            }
+          } else {
+            fail = true;
+          }
+        } else {
+          fail = true;
         }
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->p_full[s]);
+      if (wg_sync_or(fail)) { ok = false; break; }
+      if (j > 0 && !rescale_check(j - 1)) { ok = false; break; }
     }
+    if (ok && n_pages > 0 && !rescale_check(n_pages - 1)) ok = false;
 
     // ------------------------------------------------------------ epilogue
-    if (row_thread) {
+    if (owner) {
       const bool has = l_sum > 0.f;
-      ctl->inv_l[r] = has ? kv_scale / l_sum : 0.f;
-      ctl->lse[r] = has ? (m_ref + lg2(l_sum)) * kLn2 : -INFINITY;
+      const float il = has ? kv_scale / l_sum : 0.f;
+      ctl->inv_l[r] = il;
+      st_cluster_u32(mapa_shared(smem_u32(&ctl->inv_l[r]), peer), __float_as_uint(il));
+      const int64_t grow = (int64_t)b * p.rows + row0 + r;
+      if (row_ok) {
+        float lv = has ? (m_ref + lg2(l_sum)) * kLn2 : -INFINITY;
+        if (poisoned || !ok) lv = NAN;
+        if (p.splits == 1) {
+          if (p.lse) p.lse[grow] = lv;
+        } else {
+          p.partials[(grow * p.splits + split) * kPartRow + kKvLora] = lv;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->fin), cta));
+        mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->fin), peer));
+      }
     }
     if (poisoned) atomicOr(&ctl->poisoned, 1);
-    // O^T is final once PV(n-1) has completed.
-    bool fail = !ok || (n_pages > 0 && !wait_bar(ctl, &ctl->empty[(n_pages - 1) & 1], ((n_pages - 1) >> 1) & 1, p, 8));
+    bool fail = !wait_bar(ctl, &ctl->fin, 0, p, 16);
+    fail |= !ok || (n_pages > 0 && !wait_bar(ctl, &ctl->empty[(n_pages - 1) & 1], ((n_pages - 1) >> 1) & 1, p, 8));
     fail = wg_sync_or(fail);
     tc_fence_after();
+    __syncwarp();
     const bool have_o = !fail && n_pages > 0;
     const bool bad = ctl->poisoned != 0 || fail;
-    __syncwarp();
     const int rows_here = min(kRows, p.rows - row0);
     const int64_t grow0 = (int64_t)b * p.rows + row0;
+    // O_c rows are TMEM lanes: stage 32 rows x 32 columns through shared memory
+    // (the S_in region, idle now) so global stores run along the 512 columns.
+    float* tile = reinterpret_cast<float*>(sSin) + (warp - kSoftmaxWarp0) * (32 * 33);
+    const float il = ctl->inv_l[r];
 #pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      const int dim = blk * 128 + quad * 32 + lane;
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        uint32_t v[16];
-        if (have_o) {
-          tmem_ld16(tmem + lane_base + kColO + blk * 64 + g * 16, v);
-          tmem_ld_wait();
-        }
+    for (int c0 = 0; c0 < 256; c0 += 32) {
+      uint32_t v[2][16];
+      if (have_o) {
+        tmem_ld16(tmem + lane_base + kColO + c0, v[0]);
+        tmem_ld16(tmem + lane_base + kColO + c0 + 16, v[1]);
+        tmem_ld_wait();
+      }
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int rr = g * 16 + k;
-          if (rr >= rows_here) continue;
-          const float il = ctl->inv_l[rr];
-          float o = (have_o && il > 0.f) ? __uint_as_float(v[k]) * il : 0.f;
-          if (bad) o = NAN;
-          const int64_t grow = grow0 + rr;
-          if (p.splits == 1)
-            store_out(p, grow, dim, o);
-          else
-            p.partials[(grow * p.splits + split) * kPartRow + dim] = o;
-        }
+      for (int k = 0; k < 32; ++k) {
+        float o = (have_o && il > 0.f) ? __uint_as_float(v[k >> 4][k & 15]) * il : 0.f;
+        if (bad) o = NAN;
+        tile[lane * 33 + k] = o;
       }
-    }
-    if (wg_t < rows_here) {
-      const int64_t grow = grow0 + wg_t;
-      const float lv = bad ? NAN : ctl->lse[wg_t];
-      if (p.splits == 1) {
-        if (p.lse) p.lse[grow] = lv;
-      } else {
-        p.partials[(grow * p.splits + split) * kPartRow + kKvLora] = lv;
+      __syncwarp();
+      const int dim = (int)cta * 256 + c0 + lane;
+#pragma unroll 4
+      for (int rr = 0; rr < 32; ++rr) {
+        const int row = quad * 32 + rr;
+        if (row >= rows_here) break;
+        const float o = tile[rr * 33 + lane];
+        const int64_t grow = grow0 + row;
+        if (p.splits == 1)
+          store_out(p, grow, dim, o);
+        else
+          p.partials[(grow * p.splits + split) * kPartRow + dim] = o;
       }
+      __syncwarp();
     }
     tc_fence_before();
   }
 
   __syncthreads();
+  cluster_sync_all();  // no remote store or arrive can target a CTA that has exited
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -547,18 +660,17 @@ EncodeFn get_encode() {
   return fn;
 }
 
-// 2-D tensor map: `rows` rows of `cols` elements, `stride_elems` apart, box 64 x 64.
+// 2-D tensor map: `rows` rows of `cols` elements, `stride_elems` apart, box 64 x box_rows.
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t stride_elems,
-               CUtensorMapDataType dt, uint32_t elem_bytes, CUtensorMapSwizzle swz) {
+               CUtensorMapDataType dt, uint32_t elem_bytes, uint32_t box_rows, CUtensorMapSwizzle swz) {
   EncodeFn enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {stride_elems * elem_bytes};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -567,17 +679,17 @@ cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
   CUtensorMap tm_qn, tm_qp, tm_kv;
   const uint64_t q_rows = (uint64_t)p.batch * p.rows;
   const uint64_t kv_rows = (uint64_t)p.num_pages * kPage;
-  if (!encode_2d(&tm_qn, p.q_nope, kKvLora, q_rows, p.q_nope_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  if (!encode_2d(&tm_qn, p.q_nope, kKvLora, q_rows, p.q_nope_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tm_qp, p.q_pe, kRope, q_rows, p.q_pe_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+      !encode_2d(&tm_qp, p.q_pe, kRope, q_rows, p.q_pe_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  const bool ok = p.kv_fp8 ? encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+  const bool ok = p.kv_fp8 ? encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64,
                                        CU_TENSOR_MAP_SWIZZLE_NONE)
-                           : encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                           : encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
                                        CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
-  const dim3 grid(p.row_groups, p.splits, p.batch);
+  const dim3 grid(2 * p.row_groups, p.splits, p.batch);
   if (p.kv_fp8) {
     auto kern = split_kv_tc_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
