@@ -84,6 +84,17 @@ constexpr int kPrefetchPages = 4;
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
 
+// Per page and owner warp: each row's O rescale factor and whether any row of
+// the warp moved its reference max (flag = page + 1).  Copied to the peer with
+// the warp's 32 P rows.
+struct alignas(16) Meta {
+  float fac[32];
+  int flag;
+  int pad[3];
+};
+constexpr int kMetaBytes = sizeof(Meta);
+constexpr uint32_t kPvReadyTx = 2 * (32 * 128 + kMetaBytes);  // the peer's 2 owner warps' copies
+
 struct Ctl {
   uint64_t q_full;
   uint64_t raw_full[kStages];
@@ -91,18 +102,18 @@ struct Ctl {
   uint64_t empty[kStages];     // this CTA's PV of the stage's page has completed
   uint64_t s_full[kStages];    // QK^T of the page is in TMEM
   uint64_t s_free[kStages];    // the 4 softmax warps have read it (count 4)
-  uint64_t sin_full[2];        // peer's 2 sender warps delivered partial S (count 2, remote)
+  uint64_t sin_full[2];        // peer's partial S landed (count 1 + 16 KB of st.async bytes)
   uint64_t sin_free[2];        // peer's 2 owner warps consumed what this CTA sent (count 2, remote)
   uint64_t p_free[2];          // PV of the buffer's previous page done in both CTAs (count 2)
-  uint64_t pv_ready[2];        // both CTAs' owners wrote P (count 4: 2 local + 2 remote)
+  uint64_t pv_ready[2];        // local owners wrote P (count 2) + the peer's P and meta copies landed
   uint64_t rescaled[2];        // the 4 local warps rescaled O (count 4)
   uint64_t fin;                // 1/l of all 128 rows delivered (count 4)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int poisoned;
-  int flag[2];                 // page+1 when some row of that page needs O rescaled
-  float fac[2][kRows];
+  Meta meta_local[2][2];       // [page buffer][owner warp]: written by this CTA's owners
+  Meta meta_peer[2][2];        // the same, copied in from the peer
   float inv_l[kRows];
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
@@ -211,12 +222,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       mbar_init(&ctl->s_free[s], 4);
     }
     for (int e = 0; e < 2; ++e) {
-      mbar_init(&ctl->sin_full[e], 2);
+      mbar_init(&ctl->sin_full[e], 1);
       mbar_init(&ctl->sin_free[e], 2);
       mbar_init(&ctl->p_free[e], 2);
-      mbar_init(&ctl->pv_ready[e], 4);
+      mbar_init(&ctl->pv_ready[e], 2);
       mbar_init(&ctl->rescaled[e], 4);
-      ctl->flag[e] = 0;
+      for (int w = 0; w < 2; ++w) ctl->meta_local[e][w].flag = ctl->meta_peer[e][w].flag = 0;
     }
     mbar_init(&ctl->fin, 4);
     mbar_init(&ctl->drain, 1);
@@ -302,7 +313,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       auto issue_pv = [&](int j) -> bool {
         const int e = j & 1;
         if (!wait_bar(ctl, &ctl->pv_ready[e], (j >> 1) & 1, p, 5)) return false;
-        if (*(volatile int*)&ctl->flag[e] == j + 1) {  // some row's reference max moved
+        const volatile Meta* ml = ctl->meta_local[e];
+        const volatile Meta* mp = ctl->meta_peer[e];
+        if (ml[0].flag == j + 1 || ml[1].flag == j + 1 || mp[0].flag == j + 1 ||
+            mp[1].flag == j + 1) {  // some row's reference max moved
           if (!wait_bar(ctl, &ctl->rescaled[e], nres[e] & 1, p, 10)) return false;
           ++nres[e];
         }
@@ -395,28 +409,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t sin_local = smem_u32(sSin);
     const uint32_t sin_peer = mapa_shared(sin_local, peer);
-    const uint32_t p_local = smem_u32(sP);
-    const uint32_t p_peer = mapa_shared(p_local, peer);
+    const uint32_t p_peer = mapa_shared(smem_u32(sP), peer);
+    const int ow = quad & 1;  // owner-warp index of this quadrant (CTA 0: quads 0,1; CTA 1: quads 2,3)
     float m_ref = -INFINITY, l_sum = 0.f;
     bool poisoned = !len_ok;
     bool ok = true;
-    int nres[2] = {0, 0};
 
-    // Rescale check for page jj, run one page later so senders never wait on it:
-    // if any row of either CTA moved its reference max on page jj, every warp
-    // rescales its lanes of O (rows) by fac before PV(jj) is issued.
+    // Every warp runs this loop on its own: decisions after a bounded wait are
+    // made warp-uniform (__all_sync), and no named barrier sits inside the loop,
+    // so sender warps run a page ahead of the owners and a warp that gives up
+    // cannot strand the others on a barrier.
+    //
+    // Rescale check for page jj, run one page later: once both CTAs' owners have
+    // written P(jj), if any row of either CTA moved its reference max on page jj,
+    // each warp rescales its lanes (rows) of O by fac before PV(jj) is issued.
     auto rescale_check = [&](int jj) -> bool {
       const int e = jj & 1;
-      bool fail = !wait_bar(ctl, &ctl->pv_ready[e], (jj >> 1) & 1, p, 11);
-      if (wg_sync_or(fail)) return false;
-      const bool resc = wg_sync_or(*(volatile int*)&ctl->flag[e] == jj + 1);
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->pv_ready[e], (jj >> 1) & 1, p, 11))) return false;
+      const volatile Meta* ml = ctl->meta_local[e];
+      const volatile Meta* mp = ctl->meta_peer[e];
+      const bool resc = ml[0].flag == jj + 1 || ml[1].flag == jj + 1 || mp[0].flag == jj + 1 || mp[1].flag == jj + 1;
       if (!resc) return true;
       // O holds pages < jj once PV(jj-1) has completed (its commit covers all before).
-      fail = jj > 0 && !wait_bar(ctl, &ctl->empty[(jj - 1) & 1], ((jj - 1) >> 1) & 1, p, 12);
-      if (wg_sync_or(fail)) return false;
+      if (jj > 0 &&
+          !__all_sync(0xffffffffu, wait_bar(ctl, &ctl->empty[(jj - 1) & 1], ((jj - 1) >> 1) & 1, p, 12)))
+        return false;
       tc_fence_after();
       __syncwarp();
-      const float f = ctl->fac[e][r];
+      const float f = owner ? ctl->meta_local[e][ow].fac[lane] : ctl->meta_peer[e][ow].fac[lane];
 #pragma unroll 1
       for (int g = 0; g < 16; ++g) {
         uint32_t v[16];
@@ -431,7 +451,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->rescaled[e]);
-      ++nres[e];
       return true;
     };
 
@@ -441,9 +460,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       const int page = bt_row[j];
       const bool page_ok = page >= 0 && page < p.num_pages;
       poisoned |= !page_ok;
-      if (wg_sync_or(!wait_bar(ctl, &ctl->s_full[s], (j >> 1) & 1, p, 6))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[s], (j >> 1) & 1, p, 6))) { ok = false; break; }
       tc_fence_after();
-      __syncwarp();
       float sv[64];
       {
         uint32_t raw[4][16];
@@ -459,113 +477,116 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->s_free[s]);
 
-      bool fail = false;
       if (!owner) {
-        // ---- sender: partial S of a row the peer owns -> peer's S_in[e][ri]
-        if (wait_bar(ctl, &ctl->sin_free[s], ((j >> 1) & 1) ^ 1, p, 13)) {
-          const uint32_t dst = sin_peer + s * kSinBytes + ri * 256;
-#pragma unroll
-          for (int u = 0; u < 16; ++u)
-            st_cluster_v4(dst + ((u ^ (ri & 7)) << 4),
-                          make_uint4(__float_as_uint(sv[4 * u]), __float_as_uint(sv[4 * u + 1]),
-                                     __float_as_uint(sv[4 * u + 2]), __float_as_uint(sv[4 * u + 3])));
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->sin_full[s]), peer));
-        } else {
-          fail = true;
+        // ---- sender: partial S of a row the peer owns -> peer's S_in[s][ri]
+        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_free[s], ((j >> 1) & 1) ^ 1, p, 13))) {
+          ok = false;
+          break;
         }
+        const uint32_t dst = sin_peer + s * kSinBytes + ri * 256;
+        const uint32_t bar = mapa_shared(smem_u32(&ctl->sin_full[s]), peer);
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          st_async_v4(dst + ((u ^ (ri & 7)) << 4),
+                      make_uint4(__float_as_uint(sv[4 * u]), __float_as_uint(sv[4 * u + 1]),
+                                 __float_as_uint(sv[4 * u + 2]), __float_as_uint(sv[4 * u + 3])),
+                      bar);
       } else {
         // ---- owner: add the peer's partial, softmax, P into both CTAs
-        if (wait_bar(ctl, &ctl->sin_full[s], (j >> 1) & 1, p, 14)) {
-          const float4* src = reinterpret_cast<const float4*>(sSin + s * kSinBytes + ri * 256);
+        // The peer's two sender warps deliver 16 KB of st.async bytes per page.
+        if (ow == 0 && lane == 0) mbar_arrive_expect_tx(&ctl->sin_full[s], kSinBytes);
+        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_full[s], (j >> 1) & 1, p, 14))) {
+          ok = false;
+          break;
+        }
+        const float4* src = reinterpret_cast<const float4*>(sSin + s * kSinBytes + ri * 256);
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const float4 v = src[u ^ (ri & 7)];
-            sv[4 * u] += v.x;
-            sv[4 * u + 1] += v.y;
-            sv[4 * u + 2] += v.z;
-            sv[4 * u + 3] += v.w;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->sin_free[s]), peer));
+        for (int u = 0; u < 16; ++u) {
+          const float4 v = src[u ^ (ri & 7)];
+          sv[4 * u] += v.x;
+          sv[4 * u + 1] += v.y;
+          sv[4 * u + 2] += v.z;
+          sv[4 * u + 3] += v.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&ctl->sin_free[s]), peer));
 
-          // V rows of tokens at or past L (or of a page that was never loaded) may
-          // hold anything, NaN included; zero this CTA's 256 V columns of them.
-          const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
-          if (ri >= n_valid) {
-            uint8_t* stage = sKV + s * kStageBytes;
+        // V rows of tokens at or past L (or of a page that was never loaded) may
+        // hold anything, NaN included; zero this CTA's 256 V columns of them.
+        const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
+        if (ri >= n_valid) {
+          uint8_t* stage = sKV + s * kStageBytes;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint4* rowp = reinterpret_cast<uint4*>(stage + c * kKvChunkBytes + ri * 128);
+          for (int c = 0; c < 4; ++c) {
+            uint4* rowp = reinterpret_cast<uint4*>(stage + c * kKvChunkBytes + ri * 128);
 #pragma unroll
-              for (int u = 0; u < 8; ++u) rowp[u] = make_uint4(0, 0, 0, 0);
-            }
+            for (int u = 0; u < 8; ++u) rowp[u] = make_uint4(0, 0, 0, 0);
           }
+        }
 
-          const int n_vis = page_ok ? min(max(vis - tok0, 0), kPage) : 0;
-          float mx = -INFINITY;
+        const int n_vis = page_ok ? min(max(vis - tok0, 0), kPage) : 0;
+        float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float x = (row_ok && c < n_vis) ? sv[c] * sc2 : -INFINITY;
-            sv[c] = x;
-            mx = fmaxf(mx, x);
-          }
-          const bool need = row_ok && (mx > m_ref + kRescaleThreshold);
-          float fac = 1.f;
-          if (need) {
-            fac = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
-            l_sum *= fac;
-            m_ref = mx;
-          }
-          uint4 pk[8];
-          float part = 0.f;
+        for (int c = 0; c < 64; ++c) {
+          const float x = (row_ok && c < n_vis) ? sv[c] * sc2 : -INFINITY;
+          sv[c] = x;
+          mx = fmaxf(mx, x);
+        }
+        const bool need = row_ok && (mx > m_ref + kRescaleThreshold);
+        float fac = 1.f;
+        if (need) {
+          fac = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
+          l_sum *= fac;
+          m_ref = mx;
+        }
+        uint4 pk[8];
+        float part = 0.f;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint32_t w[4];
+        for (int u = 0; u < 8; ++u) {
+          uint32_t w[4];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
-              const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - m_ref);
-              const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - m_ref);
-              part += p0 + p1;
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-              w[h] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int h = 0; h < 4; ++h) {
+            const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
+            const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - m_ref);
+            const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - m_ref);
+            part += p0 + p1;
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            w[h] = *reinterpret_cast<uint32_t*>(&b2);
           }
-          l_sum += part;
-          // Both CTAs' PV of page j-2 must be done before P buffer s is rewritten.
-          if (wait_bar(ctl, &ctl->p_free[s], ((j >> 1) & 1) ^ 1, p, 15)) {
-            const uint32_t off = s * kPBytes + r * 128;
+          pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l_sum += part;
+        // Both CTAs' PV of page j-2 must be done before P buffer s is rewritten.
+        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->p_free[s], ((j >> 1) & 1) ^ 1, p, 15))) {
+          ok = false;
+          break;
+        }
+        const uint32_t off = s * kPBytes + r * 128;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint32_t o = off + ((u ^ (r & 7)) << 4);
-              *reinterpret_cast<uint4*>(sP + o) = pk[u];
-              st_cluster_v4(p_peer + o, pk[u]);
-            }
-            ctl->fac[s][r] = fac;
-            st_cluster_u32(mapa_shared(smem_u32(&ctl->fac[s][r]), peer), __float_as_uint(fac));
-            if (need && j > 0) {  // page 0's PV overwrites O, so it never needs a rescale
-              ctl->flag[s] = j + 1;
-              st_cluster_u32(mapa_shared(smem_u32(&ctl->flag[s]), peer), (uint32_t)(j + 1));
-            }
-            fence_proxy_async_cluster();
-            __syncwarp();
-            if (lane == 0) {
-              mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->pv_ready[s]), cta));
-              mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->pv_ready[s]), peer));
-            }
-          } else {
-            fail = true;
-          }
-        } else {
-          fail = true;
+        for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(sP + off + ((u ^ (r & 7)) << 4)) = pk[u];
+        Meta& me = ctl->meta_local[s][ow];
+        me.fac[lane] = fac;
+        const bool any_need = __any_sync(0xffffffffu, need) && j > 0;  // page 0's PV overwrites O
+        if (lane == 0) me.flag = any_need ? j + 1 : 0;
+        fence_proxy_async_smem();  // P rows and meta visible to the MMA and the bulk copy engine
+        __syncwarp();
+        if (lane == 0) {
+          // This warp's 32 P rows (4 KB, contiguous) and its meta go to the peer
+          // through the async proxy; the peer's pv_ready counts the bytes.
+          const uint32_t bar = mapa_shared(smem_u32(&ctl->pv_ready[s]), peer);
+          const uint32_t rows_off = s * kPBytes + quad * 32 * 128;
+          bulk_copy_to_peer(p_peer + rows_off, sP + rows_off, 32 * 128, bar);
+          bulk_copy_to_peer(mapa_shared(smem_u32(&ctl->meta_peer[s][ow]), peer), &me, kMetaBytes, bar);
+          if (ow == 0)
+            mbar_arrive_expect_tx(&ctl->pv_ready[s], kPvReadyTx);
+          else
+            mbar_arrive(&ctl->pv_ready[s]);
         }
       }
-      if (wg_sync_or(fail)) { ok = false; break; }
       if (j > 0 && !rescale_check(j - 1)) { ok = false; break; }
     }
     if (ok && n_pages > 0 && !rescale_check(n_pages - 1)) ok = false;
+    ok = !wg_sync_or(!ok);  // the epilogue decides as one group
 
     // ------------------------------------------------------------ epilogue
     if (owner) {
