@@ -20,7 +20,7 @@
 //
 // Warp roles (192 threads; 320 for an FP8 cache):
 //   warp 0     TMA producer: Q once, then per page a block-table lookup and the
-//              CTA's 4 or 5 64x64 boxes (128B swizzle) into a 2-stage ring; L2
+//              CTA's 4 or 5 64x64 boxes (128B swizzle) into a 4-stage ring; L2
 //              prefetch of upcoming pages; owns the TMEM allocation.
 //   warp 1     MMA issuer (one thread).
 //   warps 2-5  softmax / exchange / epilogue warpgroup.  Warp w reads TMEM lane
@@ -35,7 +35,9 @@
 //              bf16) in the swizzled layout.  The per-tensor scale is folded into
 //              the softmax scale and the epilogue.
 //
-// TMEM: S double buffer at columns [0,128), O_c at [128, 384).
+// Q_c is kept in tensor memory as the A operand of QK^T (it is read every page;
+// from TMEM it costs no shared-memory bandwidth and frees room for 4 page stages).
+// TMEM: O_c at columns [0,256), S at [256,320), Q_c at [320, 480).
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -53,11 +55,12 @@ constexpr int kMaxCh = 5;               // 64-column chunks a CTA holds (CTA 0: 
 constexpr int kQChunkBytes = 128 * 128;  // 128 rows x 128 B
 constexpr int kKvChunkBytes = 64 * 128;  // 64 tokens x 128 B
 constexpr int kStageBytes = kMaxCh * kKvChunkBytes;
-constexpr int kStages = 2;
+constexpr int kStages = 4;
 constexpr int kSinBytes = 64 * 64 * 4;  // peer's partial S for the 64 owned rows
 constexpr int kPBytes = kRows * 128;    // P[128 rows x 64 tokens] bf16
-constexpr int kQOff = 0;
-constexpr int kStageOff = kQOff + kMaxCh * kQChunkBytes;
+constexpr int kStageOff = 0;
+constexpr int kQStageOff = kStageOff + 2 * kStageBytes;  // Q lands in stages 2-3 before moving to TMEM
+static_assert(kMaxCh * kQChunkBytes <= 2 * kStageBytes, "Q staging");
 constexpr int kSinOff = kStageOff + kStages * kStageBytes;
 constexpr int kPOff = kSinOff + 2 * kSinBytes;
 constexpr int kCtlOff = kPOff + 2 * kPBytes;
@@ -67,8 +70,9 @@ static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kPOff % 1024 == 0 && kStageOff % 1024 == 0, "swizzle atoms");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // two 64-column S buffers
-constexpr uint32_t kColO = 128;  // O_c: 256 columns
+constexpr uint32_t kColO = 0;    // O_c: 256 columns
+constexpr uint32_t kColS = 256;  // S: 64 columns
+constexpr uint32_t kColQ = 320;  // Q_c as the A operand: 2 bf16 per column, up to 160 columns
 
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kConvWarp0 = 6;
@@ -100,8 +104,9 @@ struct Ctl {
   uint64_t raw_full[kStages];
   uint64_t full[kStages];
   uint64_t empty[kStages];     // this CTA's PV of the stage's page has completed
-  uint64_t s_full[kStages];    // QK^T of the page is in TMEM
-  uint64_t s_free[kStages];    // the 4 softmax warps have read it (count 4)
+  uint64_t q_tmem;             // Q moved from shared to tensor memory (count 4)
+  uint64_t s_full;             // QK^T of the page is in TMEM
+  uint64_t s_free;             // the 4 softmax warps have read it (count 4)
   uint64_t sin_full[2];        // peer's partial S landed (count 1 + 16 KB of st.async bytes)
   uint64_t sin_free[2];        // peer's 2 owner warps consumed what this CTA sent (count 2, remote)
   uint64_t p_free[2];          // PV of the buffer's previous page done in both CTAs (count 2)
@@ -187,7 +192,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
-  uint8_t* sQ = smem + kQOff;
+  uint8_t* sQ = smem + kQStageOff;  // Q staging (then stages 2-3)
   uint8_t* sKV = smem + kStageOff;
   uint8_t* sSin = smem + kSinOff;
   uint8_t* sP = smem + kPOff;
@@ -218,9 +223,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       mbar_init(&ctl->raw_full[s], 1);
       mbar_init(&ctl->full[s], kFp8 ? 4 : 1);
       mbar_init(&ctl->empty[s], 1);
-      mbar_init(&ctl->s_full[s], 1);
-      mbar_init(&ctl->s_free[s], 4);
     }
+    mbar_init(&ctl->q_tmem, 4);
+    mbar_init(&ctl->s_full, 1);
+    mbar_init(&ctl->s_free, 4);
     for (int e = 0; e < 2; ++e) {
       mbar_init(&ctl->sin_full[e], 1);
       mbar_init(&ctl->sin_free[e], 2);
@@ -273,11 +279,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       int issued = 0;
       int next_page = bt_row[0];
       for (int j = 0; j < n_pages; ++j) {
-        const int s = j & 1;
+        const int s = j & 3;
         const int page = next_page;
-        if (j + 1 < n_pages) next_page = bt_row[j + 1];  // lookup ahead of the wait
-        if (!wait_bar(ctl, &ctl->empty[s], ((j >> 1) & 1) ^ 1, p, 1)) break;
-        prefetch_page(j + kPrefetchPages);
+        if (j + 1 < n_pages) next_page = bt_row[j + 1];  // lookups ahead of the waits
+        const int pf = (cta == 0 && j + kPrefetchPages < n_pages) ? bt_row[j + kPrefetchPages] : -1;
+        // Stages 2-3 hold Q until the softmax warps have moved it into TMEM.
+        if (j == 2 && !wait_bar(ctl, &ctl->q_tmem, 0, p, 17)) break;
+        if (!wait_bar(ctl, &ctl->empty[s], ((j >> 2) & 1) ^ 1, p, 1)) break;
+        if (pf >= 0 && pf < p.num_pages)
+          prefetch_l2(static_cast<const uint8_t*>(p.kv) + pf * page_bytes, (uint32_t)page_bytes);
         uint64_t* land = kFp8 ? &ctl->raw_full[s] : &ctl->full[s];
         uint8_t* stage = sKV + s * kStageBytes;
         if (page < 0 || page >= p.num_pages) {
@@ -296,20 +306,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       }
       // Never leave with copies in flight.
       for (int j = max(0, issued - kStages); j < issued; ++j) {
-        uint64_t* land = kFp8 ? &ctl->raw_full[j & 1] : &ctl->full[j & 1];
+        uint64_t* land = kFp8 ? &ctl->raw_full[j & 3] : &ctl->full[j & 3];
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(land), (j >> 1) & 1))
+        while (!mbar_try_wait(smem_u32(land), (j >> 2) & 1))
           if (globaltimer_ns() - t0 > kWaitLimitNs) break;
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_pages > 0) {
-      const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint32_t kv_addr = smem_u32(sKV);
       const uint32_t p_addr = smem_u32(sP);
       int nres[2] = {0, 0};
-      bool ok = wait_bar(ctl, &ctl->q_full, 0, p, 2);
+      bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
       auto issue_pv = [&](int j) -> bool {
         const int e = j & 1;
         if (!wait_bar(ctl, &ctl->pv_ready[e], (j >> 1) & 1, p, 5)) return false;
@@ -321,30 +330,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
           ++nres[e];
         }
         tc_fence_after();
-        const uint64_t v_desc = sdesc_sw128(kv_addr + e * kStageBytes, kKvChunkBytes, 1024);
+        const uint64_t v_desc = sdesc_sw128(kv_addr + (j & 3) * kStageBytes, kKvChunkBytes, 1024);
         const uint64_t p_desc = sdesc_sw128(p_addr + e * kPBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_bf16_ss(tmem + kColO, p_desc + (uint64_t)((kk * 32) >> 4), v_desc + (uint64_t)((kk * 2048) >> 4),
                       kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&ctl->empty[e]);               // stage free; O current through page j
+        mma_commit(&ctl->empty[j & 3]);           // stage free; O current through page j
         mma_commit_multicast(&ctl->p_free[e], 3);  // P buffer e reusable, in both CTAs
         return true;
       };
       for (int j = 0; ok && j < n_pages; ++j) {
-        const int s = j & 1;
-        if (!wait_bar(ctl, &ctl->full[s], (j >> 1) & 1, p, 3)) { ok = false; break; }
-        if (!wait_bar(ctl, &ctl->s_free[s], ((j >> 1) & 1) ^ 1, p, 4)) { ok = false; break; }
+        const int s = j & 3;
+        if (!wait_bar(ctl, &ctl->full[s], (j >> 2) & 1, p, 3)) { ok = false; break; }
+        if (!wait_bar(ctl, &ctl->s_free, (j & 1) ^ 1, p, 4)) { ok = false; break; }
         tc_fence_after();
         const uint64_t k_desc = sdesc_sw128(kv_addr + s * kStageBytes, 16, 1024);
-        const uint32_t d = tmem + kColS + s * 64;
         for (int k = 0; k < nch; ++k) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(d, q_desc + (uint64_t)((k * kQChunkBytes + kk * 32) >> 4),
+          for (int kk = 0; kk < 4; ++kk)  // A = Q_c from TMEM: 16 k per MMA = 8 columns
+            mma_bf16_ts(tmem + kColS, tmem + kColQ + k * 32 + kk * 8,
                         k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4), kIdescQK, (k | kk) ? 1u : 0u);
         }
-        mma_commit(&ctl->s_full[s]);
+        mma_commit(&ctl->s_full);
         if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok) issue_pv(n_pages - 1);
@@ -358,8 +366,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
     const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
     const int units = nch * 64;                    // (chunk, token) pairs of 64 bytes
     for (int j = 0; j < n_pages; ++j) {
-      const int s = j & 1;
-      if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[s], (j >> 1) & 1, p, 9))) break;
+      const int s = j & 3;
+      if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[s], (j >> 2) & 1, p, 9))) break;
       uint8_t* stage = sKV + s * kStageBytes;
       uint4 raw[3][4];
 #pragma unroll
@@ -432,7 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       if (!resc) return true;
       // O holds pages < jj once PV(jj-1) has completed (its commit covers all before).
       if (jj > 0 &&
-          !__all_sync(0xffffffffu, wait_bar(ctl, &ctl->empty[(jj - 1) & 1], ((jj - 1) >> 1) & 1, p, 12)))
+          !__all_sync(0xffffffffu, wait_bar(ctl, &ctl->empty[(jj - 1) & 3], ((jj - 1) >> 2) & 1, p, 12)))
         return false;
       tc_fence_after();
       __syncwarp();
@@ -454,19 +462,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       return true;
     };
 
-    for (int j = 0; j < n_pages; ++j) {
-      const int s = j & 1;
+    // Q_c rows into tensor memory: thread = row = TMEM lane; the 128B-swizzled
+    // staging rows are un-swizzled into 2-bf16 columns, 32 columns per chunk.
+    if (n_pages > 0) {
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->q_full, 0, p, 18))) {
+        ok = false;
+      } else {
+        for (int k = 0; k < nch; ++k) {
+          const uint8_t* qrow = sQ + k * kQChunkBytes + r * 128;
+          uint32_t w[2][16];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((u ^ (r & 7)) << 4));
+            w[u >> 2][(u & 3) * 4 + 0] = v.x;
+            w[u >> 2][(u & 3) * 4 + 1] = v.y;
+            w[u >> 2][(u & 3) * 4 + 2] = v.z;
+            w[u >> 2][(u & 3) * 4 + 3] = v.w;
+          }
+          tmem_st16(tmem + lane_base + kColQ + k * 32, w[0]);
+          tmem_st16(tmem + lane_base + kColQ + k * 32 + 16, w[1]);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->q_tmem);
+    }
+
+    for (int j = 0; ok && j < n_pages; ++j) {
+      const int s = j & 1;   // exchange buffers (S_in, P, meta)
+      const int st = j & 3;  // page stage
       const int tok0 = lo + j * kPage;  // lo is page aligned
       const int page = bt_row[j];
       const bool page_ok = page >= 0 && page < p.num_pages;
       poisoned |= !page_ok;
-      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[s], (j >> 1) & 1, p, 6))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full, j & 1, p, 6))) { ok = false; break; }
       tc_fence_after();
       float sv[64];
       {
         uint32_t raw[4][16];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) tmem_ld16(tmem + lane_base + kColS + s * 64 + g * 16, raw[g]);
+        for (int g = 0; g < 4; ++g) tmem_ld16(tmem + lane_base + kColS + g * 16, raw[g]);
         tmem_ld_wait();
 #pragma unroll
         for (int g = 0; g < 4; ++g)
@@ -475,7 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->s_free[s]);
+      if (lane == 0) mbar_arrive(&ctl->s_free);
 
       if (!owner) {
         // ---- sender: partial S of a row the peer owns -> peer's S_in[s][ri]
@@ -515,7 +551,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
         // hold anything, NaN included; zero this CTA's 256 V columns of them.
         const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
         if (ri >= n_valid) {
-          uint8_t* stage = sKV + s * kStageBytes;
+          uint8_t* stage = sKV + st * kStageBytes;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint4* rowp = reinterpret_cast<uint4*>(stage + c * kKvChunkBytes + ri * 128);
@@ -612,7 +648,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
     }
     if (poisoned) atomicOr(&ctl->poisoned, 1);
     bool fail = !wait_bar(ctl, &ctl->fin, 0, p, 16);
-    fail |= !ok || (n_pages > 0 && !wait_bar(ctl, &ctl->empty[(n_pages - 1) & 1], ((n_pages - 1) >> 1) & 1, p, 8));
+    fail |= !ok || (n_pages > 0 && !wait_bar(ctl, &ctl->empty[(n_pages - 1) & 3], ((n_pages - 1) >> 2) & 1, p, 8));
     fail = wg_sync_or(fail);
     tc_fence_after();
     __syncwarp();
