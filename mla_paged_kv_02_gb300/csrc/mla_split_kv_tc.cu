@@ -428,9 +428,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
     // so sender warps run a page ahead of the owners and a warp that gives up
     // cannot strand the others on a barrier.
     //
-    // Rescale check for page jj, run one page later: once both CTAs' owners have
-    // written P(jj), if any row of either CTA moved its reference max on page jj,
-    // each warp rescales its lanes (rows) of O by fac before PV(jj) is issued.
+    // Rescale check for page jj, run at the start of iteration jj+2 (by then both
+    // CTAs' P(jj) has long been written, so the wait is free): if any row of either
+    // CTA moved its reference max on page jj, each warp rescales its lanes (rows)
+    // of O by fac before PV(jj) is issued.  It precedes the wait for S(jj+2):
+    // PV(jj) is issued before QK(jj+2), so waiting for S first could deadlock.
     auto rescale_check = [&](int jj) -> bool {
       const int e = jj & 1;
       if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->pv_ready[e], (jj >> 1) & 1, p, 11))) return false;
@@ -496,6 +498,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       const int page = bt_row[j];
       const bool page_ok = page >= 0 && page < p.num_pages;
       poisoned |= !page_ok;
+      if (j >= 2 && !rescale_check(j - 2)) { ok = false; break; }
       if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full, j & 1, p, 6))) { ok = false; break; }
       tc_fence_after();
       float sv[64];
@@ -535,15 +538,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
           ok = false;
           break;
         }
+        // Full score = own partial + the peer's partial; mask and scale into the
+        // exp2 domain while reducing the row max over four independent chains.
         const float4* src = reinterpret_cast<const float4*>(sSin + s * kSinBytes + ri * 256);
+        const int n_vis = (page_ok && row_ok) ? min(max(vis - tok0, 0), kPage) : 0;
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const float4 v = src[u ^ (ri & 7)];
-          sv[4 * u] += v.x;
-          sv[4 * u + 1] += v.y;
-          sv[4 * u + 2] += v.z;
-          sv[4 * u + 3] += v.w;
+          const float a[4] = {sv[4 * u] + v.x, sv[4 * u + 1] + v.y, sv[4 * u + 2] + v.z, sv[4 * u + 3] + v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float x = (4 * u + k < n_vis) ? a[k] * sc2 : -INFINITY;
+            sv[4 * u + k] = x;
+            mq[k] = fmaxf(mq[k], x);
+          }
         }
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&ctl->sin_free[s]), peer));
 
@@ -560,14 +571,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
           }
         }
 
-        const int n_vis = page_ok ? min(max(vis - tok0, 0), kPage) : 0;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float x = (row_ok && c < n_vis) ? sv[c] * sc2 : -INFINITY;
-          sv[c] = x;
-          mx = fmaxf(mx, x);
-        }
         const bool need = row_ok && (mx > m_ref + kRescaleThreshold);
         float fac = 1.f;
         if (need) {
@@ -576,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
           m_ref = mx;
         }
         uint4 pk[8];
-        float part = 0.f;
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           uint32_t w[4];
@@ -585,13 +588,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
             const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
             const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - m_ref);
             const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - m_ref);
-            part += p0 + p1;
+            part[h] += p0 + p1;
             __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
             w[h] = *reinterpret_cast<uint32_t*>(&b2);
           }
           pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l_sum += part;
+        l_sum += (part[0] + part[1]) + (part[2] + part[3]);
         // Both CTAs' PV of page j-2 must be done before P buffer s is rewritten.
         if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->p_free[s], ((j >> 1) & 1) ^ 1, p, 15))) {
           ok = false;
@@ -619,9 +622,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
             mbar_arrive(&ctl->pv_ready[s]);
         }
       }
-      if (j > 0 && !rescale_check(j - 1)) { ok = false; break; }
     }
-    if (ok && n_pages > 0 && !rescale_check(n_pages - 1)) ok = false;
+    if (ok && n_pages >= 2 && !rescale_check(n_pages - 2)) ok = false;
+    if (ok && n_pages >= 1 && !rescale_check(n_pages - 1)) ok = false;
     ok = !wg_sync_or(!ok);  // the epilogue decides as one group
 
     // ------------------------------------------------------------ epilogue
