@@ -538,23 +538,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
           ok = false;
           break;
         }
-        // Full score = own partial + the peer's partial; mask and scale into the
-        // exp2 domain while reducing the row max over four independent chains.
+        // Full score = own partial + the peer's partial.  Pages that every row of
+        // the warp sees in full (all but a split's last page, normally) take a
+        // fast path: add and max on raw scores (the scale is positive, so max
+        // commutes with it), then p = 2^(s*scale - m) in one FMA + ex2.  Other
+        // pages mask and scale first; masked columns, possibly NaN garbage, become
+        // -inf and then exactly 0.
         const float4* src = reinterpret_cast<const float4*>(sSin + s * kSinBytes + ri * 256);
         const int n_vis = (page_ok && row_ok) ? min(max(vis - tok0, 0), kPage) : 0;
+        const bool fast = __all_sync(0xffffffffu, n_vis == kPage);
         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (fast) {
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float4 v = src[u ^ (ri & 7)];
-          const float a[4] = {sv[4 * u] + v.x, sv[4 * u + 1] + v.y, sv[4 * u + 2] + v.z, sv[4 * u + 3] + v.w};
+          for (int u = 0; u < 16; ++u) {
+            const float4 v = src[u ^ (ri & 7)];
+            sv[4 * u] += v.x;
+            sv[4 * u + 1] += v.y;
+            sv[4 * u + 2] += v.z;
+            sv[4 * u + 3] += v.w;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float x = (4 * u + k < n_vis) ? a[k] * sc2 : -INFINITY;
-            sv[4 * u + k] = x;
-            mq[k] = fmaxf(mq[k], x);
+            for (int k = 0; k < 4; ++k) mq[k] = fmaxf(mq[k], sv[4 * u + k]);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const float4 v = src[u ^ (ri & 7)];
+            const float a[4] = {sv[4 * u] + v.x, sv[4 * u + 1] + v.y, sv[4 * u + 2] + v.z, sv[4 * u + 3] + v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float x = (4 * u + k < n_vis) ? a[k] * sc2 : -INFINITY;
+              sv[4 * u + k] = x;
+              mq[k] = fmaxf(mq[k], x);
+            }
           }
         }
-        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        if (fast) mx *= sc2;
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&ctl->sin_free[s]), peer));
 
@@ -580,19 +599,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
         }
         uint4 pk[8];
         float part[4] = {0.f, 0.f, 0.f, 0.f};
+        if (fast) {
+          const float nm = -m_ref;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint32_t w[4];
+          for (int u = 0; u < 8; ++u) {
+            uint32_t w[4];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
-            const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - m_ref);
-            const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - m_ref);
-            part[h] += p0 + p1;
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-            w[h] = *reinterpret_cast<uint32_t*>(&b2);
+            for (int h = 0; h < 4; ++h) {
+              const float p0 = ex2(fmaf(sv[u * 8 + 2 * h], sc2, nm));
+              const float p1 = ex2(fmaf(sv[u * 8 + 2 * h + 1], sc2, nm));
+              part[h] += p0 + p1;
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              w[h] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
+              const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - m_ref);
+              const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - m_ref);
+              part[h] += p0 + p1;
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              w[h] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
         l_sum += (part[0] + part[1]) + (part[2] + part[3]);
         // Both CTAs' PV of page j-2 must be done before P buffer s is rewritten.
