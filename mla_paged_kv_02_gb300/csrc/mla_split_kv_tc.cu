@@ -491,12 +491,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       if (lane == 0) mbar_arrive(&ctl->q_tmem);
     }
 
+    // Block-table entries are loaded one page ahead: a global load consumed in
+    // the same iteration would stall every page for a full memory latency.
+    int page_next = (n_pages > 0 && owner) ? bt_row[0] : 0;
     for (int j = 0; ok && j < n_pages; ++j) {
       const int s = j & 1;   // exchange buffers (S_in, P, meta)
       const int st = j & 3;  // page stage
       const int tok0 = lo + j * kPage;  // lo is page aligned
-      const int page = bt_row[j];
-      const bool page_ok = page >= 0 && page < p.num_pages;
+      const int page = page_next;
+      if (owner && j + 1 < n_pages) page_next = bt_row[j + 1];
+      const bool page_ok = !owner || (page >= 0 && page < p.num_pages);  // only owners use it
       poisoned |= !page_ok;
       if (j >= 2 && !rescale_check(j - 2)) { ok = false; break; }
       if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full, j & 1, p, 6))) { ok = false; break; }
