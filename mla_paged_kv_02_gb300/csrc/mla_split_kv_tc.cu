@@ -319,43 +319,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       const uint32_t p_addr = smem_u32(sP);
       int nres[2] = {0, 0};
       bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
-      auto issue_pv = [&](int j) -> bool {
-        const int e = j & 1;
-        if (!wait_bar(ctl, &ctl->pv_ready[e], (j >> 1) & 1, p, 5)) return false;
-        const volatile Meta* ml = ctl->meta_local[e];
-        const volatile Meta* mp = ctl->meta_peer[e];
-        if (ml[0].flag == j + 1 || ml[1].flag == j + 1 || mp[0].flag == j + 1 ||
-            mp[1].flag == j + 1) {  // some row's reference max moved
-          if (!wait_bar(ctl, &ctl->rescaled[e], nres[e] & 1, p, 10)) return false;
-          ++nres[e];
-        }
-        tc_fence_after();
-        const uint64_t v_desc = sdesc_sw128(kv_addr + (j & 3) * kStageBytes, kKvChunkBytes, 1024);
-        const uint64_t p_desc = sdesc_sw128(p_addr + e * kPBytes, 16, 1024);
+      // Greedy issue: QK(nq) as soon as its page has landed and S is free, PV(np)
+      // as soon as both CTAs' P(np) is in (and O rescaled, if flagged).  Polling
+      // with non-blocking tests keeps one pending PV from holding back the next
+      // page's QK.  The stage ring, S, S_in and P barriers bound how far QK runs
+      // ahead.
+      int nq = 0, np = 0;
+      int resc_state = 0;  // for page np: 0 = flags not read, 1 = no rescale, 2 = waiting for rescale
+      uint64_t t_last = globaltimer_ns();
+      while (ok && np < n_pages) {
+        bool progressed = false;
+        if (nq < n_pages && mbar_test_wait_cluster(smem_u32(&ctl->full[nq & 3]), (nq >> 2) & 1) &&
+            mbar_test_wait_cluster(smem_u32(&ctl->s_free), (nq & 1) ^ 1)) {
+          tc_fence_after();
+          const uint64_t k_desc = sdesc_sw128(kv_addr + (nq & 3) * kStageBytes, 16, 1024);
+          for (int k = 0; k < nch; ++k) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ss(tmem + kColO, p_desc + (uint64_t)((kk * 32) >> 4), v_desc + (uint64_t)((kk * 2048) >> 4),
-                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&ctl->empty[j & 3]);           // stage free; O current through page j
-        mma_commit_multicast(&ctl->p_free[e], 3);  // P buffer e reusable, in both CTAs
-        return true;
-      };
-      for (int j = 0; ok && j < n_pages; ++j) {
-        const int s = j & 3;
-        if (!wait_bar(ctl, &ctl->full[s], (j >> 2) & 1, p, 3)) { ok = false; break; }
-        if (!wait_bar(ctl, &ctl->s_free, (j & 1) ^ 1, p, 4)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t k_desc = sdesc_sw128(kv_addr + s * kStageBytes, 16, 1024);
-        for (int k = 0; k < nch; ++k) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // A = Q_c from TMEM: 16 k per MMA = 8 columns
-            mma_bf16_ts(tmem + kColS, tmem + kColQ + k * 32 + kk * 8,
-                        k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4), kIdescQK, (k | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)  // A = Q_c from TMEM: 16 k per MMA = 8 columns
+              mma_bf16_ts(tmem + kColS, tmem + kColQ + k * 32 + kk * 8,
+                          k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4), kIdescQK, (k | kk) ? 1u : 0u);
+          }
+          mma_commit(&ctl->s_full);
+          ++nq;
+          progressed = true;
         }
-        mma_commit(&ctl->s_full);
-        if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+        if (np < nq) {
+          const int e = np & 1;
+          if (resc_state == 0 && mbar_test_wait_cluster(smem_u32(&ctl->pv_ready[e]), (np >> 1) & 1)) {
+            const volatile Meta* ml = ctl->meta_local[e];
+            const volatile Meta* mp = ctl->meta_peer[e];
+            resc_state = (ml[0].flag == np + 1 || ml[1].flag == np + 1 || mp[0].flag == np + 1 ||
+                          mp[1].flag == np + 1) ? 2 : 1;  // some row's reference max moved
+          }
+          if (resc_state == 2 && mbar_test_wait_cluster(smem_u32(&ctl->rescaled[e]), nres[e] & 1)) {
+            ++nres[e];
+            resc_state = 1;
+          }
+          if (resc_state == 1) {
+            tc_fence_after();
+            const uint64_t v_desc = sdesc_sw128(kv_addr + (np & 3) * kStageBytes, kKvChunkBytes, 1024);
+            const uint64_t p_desc = sdesc_sw128(p_addr + e * kPBytes, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss(tmem + kColO, p_desc + (uint64_t)((kk * 32) >> 4), v_desc + (uint64_t)((kk * 2048) >> 4),
+                          kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&ctl->empty[np & 3]);           // stage free; O current through page np
+            mma_commit_multicast(&ctl->p_free[e], 3);  // P buffer e reusable, in both CTAs
+            ++np;
+            resc_state = 0;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_last = globaltimer_ns();
+        } else if (*(volatile int*)&ctl->abort) {
+          ok = false;
+        } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
+          *(volatile int*)&ctl->abort = 1;
+          report_error(p.err, MLA_ERR_TIMEOUT, blockIdx.z, 3, blockIdx.y);
+          ok = false;
+        }
       }
-      if (ok) issue_pv(n_pages - 1);
       mma_commit(&ctl->drain);  // every MMA of this thread has completed before TMEM is freed
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(smem_u32(&ctl->drain), 0))
