@@ -165,17 +165,21 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
-// Bounded wait (acquire at cluster scope) that also gives up once any role of
-// this CTA has aborted.
+// Bounded wait that also gives up once any role of this CTA has aborted.  CTA
+// scope suffices for every barrier completed by local arrives, by transaction
+// bytes (TMA, st.async, bulk copies) or by a relaxed "consumed" signal; only a
+// barrier whose remote arrivals publish generic stores needs cluster scope.
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(Ctl* c, uint64_t* bar, uint32_t parity, const DecodeParams& p,
                                          int where) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_cluster(a, parity)) return true;
+  auto test = [&]() { return kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
+  if (test()) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int k = 0; k < 32; ++k)
-      if (mbar_try_wait_cluster(a, parity)) return true;
+      if (test()) return true;
     if (*(volatile int*)&c->abort) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *(volatile int*)&c->abort = 1;
@@ -329,8 +333,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       uint64_t t_last = globaltimer_ns();
       while (ok && np < n_pages) {
         bool progressed = false;
-        if (nq < n_pages && mbar_test_wait_cluster(smem_u32(&ctl->full[nq & 3]), (nq >> 2) & 1) &&
-            mbar_test_wait_cluster(smem_u32(&ctl->s_free), (nq & 1) ^ 1)) {
+        if (nq < n_pages && mbar_test_wait(smem_u32(&ctl->full[nq & 3]), (nq >> 2) & 1) &&
+            mbar_test_wait(smem_u32(&ctl->s_free), (nq & 1) ^ 1)) {
           tc_fence_after();
           const uint64_t k_desc = sdesc_sw128(kv_addr + (nq & 3) * kStageBytes, 16, 1024);
           for (int k = 0; k < nch; ++k) {
@@ -345,13 +349,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
         }
         if (np < nq) {
           const int e = np & 1;
-          if (resc_state == 0 && mbar_test_wait_cluster(smem_u32(&ctl->pv_ready[e]), (np >> 1) & 1)) {
+          if (resc_state == 0 && mbar_test_wait(smem_u32(&ctl->pv_ready[e]), (np >> 1) & 1)) {
             const volatile Meta* ml = ctl->meta_local[e];
             const volatile Meta* mp = ctl->meta_peer[e];
             resc_state = (ml[0].flag == np + 1 || ml[1].flag == np + 1 || mp[0].flag == np + 1 ||
                           mp[1].flag == np + 1) ? 2 : 1;  // some row's reference max moved
           }
-          if (resc_state == 2 && mbar_test_wait_cluster(smem_u32(&ctl->rescaled[e]), nres[e] & 1)) {
+          if (resc_state == 2 && mbar_test_wait(smem_u32(&ctl->rescaled[e]), nres[e] & 1)) {
             ++nres[e];
             resc_state = 1;
           }
@@ -714,7 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       }
     }
     if (poisoned) atomicOr(&ctl->poisoned, 1);
-    bool fail = !wait_bar(ctl, &ctl->fin, 0, p, 16);
+    bool fail = !wait_bar<true>(ctl, &ctl->fin, 0, p, 16);
     fail |= !ok || (n_pages > 0 && !wait_bar(ctl, &ctl->empty[(n_pages - 1) & 3], ((n_pages - 1) >> 2) & 1, p, 8));
     fail = wg_sync_or(fail);
     tc_fence_after();

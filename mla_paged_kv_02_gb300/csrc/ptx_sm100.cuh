@@ -120,6 +120,17 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
                : "memory");
 }
 
+// Non-blocking test of a phase (acquire at CTA scope), for polling several barriers.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Non-blocking test of a phase (acquire at cluster scope), for polling several barriers.
 __device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
