@@ -218,6 +218,7 @@ def main():
     ap.add_argument("--workload", default="mtp3")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the request count (smaller cases of the same kernel for ncu)")
+    ap.add_argument("--force-splits", type=int, default=0, help="override the planner's split count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -233,7 +234,7 @@ def main():
     name = args.workload
     inp = synth.make_inputs(name, seed=rank_seed(list(synth.WORKLOADS).index(name), rank), device="cuda",
                             batch=args.batch)
-    pl = api.plan_for(inp)
+    pl = api.plan_for(inp, force_splits=args.force_splits)
     ws = api.alloc_workspace(pl, "cuda")
     out, lse = api.alloc_outputs(inp)
     kvs = api.kv_scale_tensor(inp)
