@@ -35,9 +35,10 @@
 //              bf16) in the swizzled layout.  The per-tensor scale is folded into
 //              the softmax scale and the epilogue.
 //
-// Q_c is kept in tensor memory as the A operand of QK^T (it is read every page;
-// from TMEM it costs no shared-memory bandwidth and frees room for 4 page stages).
-// TMEM: O_c at columns [0,256), S at [256,320), Q_c at [320, 480).
+// Q's c_kv columns are kept in tensor memory as the A operand of QK^T (read every
+// page; from TMEM they cost no shared-memory bandwidth and leave room for 4 page
+// stages); CTA 1's q_pe chunk stays in shared memory.
+// TMEM: O_c at columns [0,256), S double buffer at [256,384), Q at [384,512).
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -59,20 +60,21 @@ constexpr int kStages = 4;
 constexpr int kSinBytes = 64 * 64 * 4;  // peer's partial S for the 64 owned rows
 constexpr int kPBytes = kRows * 128;    // P[128 rows x 64 tokens] bf16
 constexpr int kStageOff = 0;
-constexpr int kQStageOff = kStageOff + 2 * kStageBytes;  // Q lands in stages 2-3 before moving to TMEM
-static_assert(kMaxCh * kQChunkBytes <= 2 * kStageBytes, "Q staging");
-constexpr int kSinOff = kStageOff + kStages * kStageBytes;
-constexpr int kPOff = kSinOff + 2 * kSinBytes;
-constexpr int kCtlOff = kPOff + 2 * kPBytes;
+constexpr int kQStageOff = kStageOff + 2 * kStageBytes;  // Q's c_kv chunks land in stages 2-3, then go to TMEM
+static_assert(4 * kQChunkBytes <= 2 * kStageBytes, "Q staging");
+constexpr int kSinOff = kStageOff + kStages * kStageBytes;  // one S_in buffer
+constexpr int kPOff = kSinOff + kSinBytes;                    // two P buffers
+constexpr int kQpeOff = kPOff + 2 * kPBytes;                  // CTA 1's q_pe chunk (A from shared memory)
+constexpr int kCtlOff = kQpeOff + kQChunkBytes;
 constexpr int kCtlBytes = 2048;
 constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory");
-static_assert(kPOff % 1024 == 0 && kStageOff % 1024 == 0, "swizzle atoms");
+static_assert(kPOff % 1024 == 0 && kStageOff % 1024 == 0 && kQpeOff % 1024 == 0, "swizzle atoms");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // O_c: 256 columns
-constexpr uint32_t kColS = 256;  // S: 64 columns
-constexpr uint32_t kColQ = 320;  // Q_c as the A operand: 2 bf16 per column, up to 160 columns
+constexpr uint32_t kColS = 256;  // S: two 64-column buffers
+constexpr uint32_t kColQ = 384;  // Q's c_kv chunks as the A operand: 2 bf16 per column, 128 columns
 
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kConvWarp0 = 6;
@@ -105,10 +107,10 @@ struct Ctl {
   uint64_t full[kStages];
   uint64_t empty[kStages];     // this CTA's PV of the stage's page has completed
   uint64_t q_tmem;             // Q moved from shared to tensor memory (count 4)
-  uint64_t s_full;             // QK^T of the page is in TMEM
-  uint64_t s_free;             // the 4 softmax warps have read it (count 4)
-  uint64_t sin_full[2];        // peer's partial S landed (count 1 + 16 KB of st.async bytes)
-  uint64_t sin_free[2];        // peer's 2 owner warps consumed what this CTA sent (count 2, remote)
+  uint64_t s_full[2];          // QK^T of the page is in TMEM
+  uint64_t s_free[2];          // the 4 softmax warps have read it (count 4)
+  uint64_t sin_full;           // peer's partial S landed (count 1 + 16 KB of st.async bytes)
+  uint64_t sin_free;           // peer's 2 owner warps consumed what this CTA sent (count 2, remote)
   uint64_t p_free[2];          // PV of the buffer's previous page done in both CTAs (count 2)
   uint64_t pv_ready[2];        // local owners wrote P (count 2) + the peer's P and meta copies landed
   uint64_t rescaled[2];        // the 4 local warps rescaled O (count 4)
@@ -199,6 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
   uint8_t* sQ = smem + kQStageOff;  // Q staging (then stages 2-3)
   uint8_t* sKV = smem + kStageOff;
   uint8_t* sSin = smem + kSinOff;
+  uint8_t* sQpe = smem + kQpeOff;
   uint8_t* sP = smem + kPOff;
 
   const int warp = threadIdx.x >> 5;
@@ -229,11 +232,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->q_tmem, 4);
-    mbar_init(&ctl->s_full, 1);
-    mbar_init(&ctl->s_free, 4);
+    mbar_init(&ctl->s_full[0], 1);
+    mbar_init(&ctl->s_full[1], 1);
+    mbar_init(&ctl->s_free[0], 4);
+    mbar_init(&ctl->s_free[1], 4);
+    mbar_init(&ctl->sin_full, 1);
+    mbar_init(&ctl->sin_free, 2);
     for (int e = 0; e < 2; ++e) {
-      mbar_init(&ctl->sin_full[e], 1);
-      mbar_init(&ctl->sin_free[e], 2);
       mbar_init(&ctl->p_free[e], 2);
       mbar_init(&ctl->pv_ready[e], 2);
       mbar_init(&ctl->rescaled[e], 4);
@@ -278,7 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
         if (g < 8)
           tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, g * 64, qrow);
         else
-          tma_load_2d(sQ + k * kQChunkBytes, &tm_qp, &ctl->q_full, 0, qrow);
+          tma_load_2d(sQpe, &tm_qp, &ctl->q_full, 0, qrow);
       }
       int issued = 0;
       int next_page = bt_row[0];
@@ -321,6 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
     if (lane == 0 && n_pages > 0) {
       const uint32_t kv_addr = smem_u32(sKV);
       const uint32_t p_addr = smem_u32(sP);
+      const uint64_t qpe_desc = sdesc_sw128(smem_u32(sQpe), 16, 1024);
       int nres[2] = {0, 0};
       bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
       // Greedy issue: QK(nq) as soon as its page has landed and S is free, PV(np)
@@ -334,16 +340,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       while (ok && np < n_pages) {
         bool progressed = false;
         if (nq < n_pages && mbar_test_wait(smem_u32(&ctl->full[nq & 3]), (nq >> 2) & 1) &&
-            mbar_test_wait(smem_u32(&ctl->s_free), (nq & 1) ^ 1)) {
+            mbar_test_wait(smem_u32(&ctl->s_free[nq & 1]), ((nq >> 1) & 1) ^ 1)) {
           tc_fence_after();
           const uint64_t k_desc = sdesc_sw128(kv_addr + (nq & 3) * kStageBytes, 16, 1024);
-          for (int k = 0; k < nch; ++k) {
+          const uint32_t d = tmem + kColS + (nq & 1) * 64;
+          for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)  // A = Q_c from TMEM: 16 k per MMA = 8 columns
-              mma_bf16_ts(tmem + kColS, tmem + kColQ + k * 32 + kk * 8,
+            for (int kk = 0; kk < 4; ++kk)  // A = Q chunk k from TMEM: 16 k per MMA = 8 columns
+              mma_bf16_ts(d, tmem + kColQ + k * 32 + kk * 8,
                           k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4), kIdescQK, (k | kk) ? 1u : 0u);
           }
-          mma_commit(&ctl->s_full);
+          if (nch == 5) {  // k_pe: A = q_pe from shared memory
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4),
+                          k_desc + (uint64_t)((4 * kKvChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
+          }
+          mma_commit(&ctl->s_full[nq & 1]);
           ++nq;
           progressed = true;
         }
@@ -498,7 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->q_full, 0, p, 18))) {
         ok = false;
       } else {
-        for (int k = 0; k < nch; ++k) {
+        for (int k = 0; k < 4; ++k) {
           const uint8_t* qrow = sQ + k * kQChunkBytes + r * 128;
           uint32_t w[2][16];
 #pragma unroll
@@ -531,13 +544,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       const bool page_ok = !owner || (page >= 0 && page < p.num_pages);  // only owners use it
       poisoned |= !page_ok;
       if (j >= 2 && !rescale_check(j - 2)) { ok = false; break; }
-      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full, j & 1, p, 6))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[s], (j >> 1) & 1, p, 6))) { ok = false; break; }
       tc_fence_after();
       float sv[64];
       {
         uint32_t raw[4][16];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) tmem_ld16(tmem + lane_base + kColS + g * 16, raw[g]);
+        for (int g = 0; g < 4; ++g) tmem_ld16(tmem + lane_base + kColS + s * 64 + g * 16, raw[g]);
         tmem_ld_wait();
 #pragma unroll
         for (int g = 0; g < 4; ++g)
@@ -546,16 +559,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->s_free);
+      if (lane == 0) mbar_arrive(&ctl->s_free[s]);
 
       if (!owner) {
         // ---- sender: partial S of a row the peer owns -> peer's S_in[s][ri]
-        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_free[s], ((j >> 1) & 1) ^ 1, p, 13))) {
+        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_free, (j & 1) ^ 1, p, 13))) {
           ok = false;
           break;
         }
-        const uint32_t dst = sin_peer + s * kSinBytes + ri * 256;
-        const uint32_t bar = mapa_shared(smem_u32(&ctl->sin_full[s]), peer);
+        const uint32_t dst = sin_peer + ri * 256;
+        const uint32_t bar = mapa_shared(smem_u32(&ctl->sin_full), peer);
 #pragma unroll
         for (int u = 0; u < 16; ++u)
           st_async_v4(dst + ((u ^ (ri & 7)) << 4),
@@ -565,8 +578,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       } else {
         // ---- owner: add the peer's partial, softmax, P into both CTAs
         // The peer's two sender warps deliver 16 KB of st.async bytes per page.
-        if (ow == 0 && lane == 0) mbar_arrive_expect_tx(&ctl->sin_full[s], kSinBytes);
-        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_full[s], (j >> 1) & 1, p, 14))) {
+        if (ow == 0 && lane == 0) mbar_arrive_expect_tx(&ctl->sin_full, kSinBytes);
+        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_full, j & 1, p, 14))) {
           ok = false;
           break;
         }
@@ -576,7 +589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
         // commutes with it), then p = 2^(s*scale - m) in one FMA + ex2.  Other
         // pages mask and scale first; masked columns, possibly NaN garbage, become
         // -inf and then exactly 0.
-        const float4* src = reinterpret_cast<const float4*>(sSin + s * kSinBytes + ri * 256);
+        const float4* src = reinterpret_cast<const float4*>(sSin + ri * 256);
         const int n_vis = (page_ok && row_ok) ? min(max(vis - tok0, 0), kPage) : 0;
         const bool fast = __all_sync(0xffffffffu, n_vis == kPage);
         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -607,7 +620,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
         float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         if (fast) mx *= sc2;
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&ctl->sin_free[s]), peer));
+        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&ctl->sin_free), peer));
 
         // V rows of tokens at or past L (or of a page that was never loaded) may
         // hold anything, NaN included; zero this CTA's 256 V columns of them.
@@ -728,8 +741,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
     const int rows_here = min(kRows, p.rows - row0);
     const int64_t grow0 = (int64_t)b * p.rows + row0;
     // O_c rows are TMEM lanes: stage 32 rows x 32 columns through shared memory
-    // (the S_in region, idle now) so global stores run along the 512 columns.
-    float* tile = reinterpret_cast<float*>(sSin) + (warp - kSoftmaxWarp0) * (32 * 33);
+    // (the P buffers, idle once the last PV has completed) so global stores run
+    // along the 512 columns.
+    float* tile = reinterpret_cast<float*>(sP) + (warp - kSoftmaxWarp0) * (32 * 33);
     const float il = ctl->inv_l[r];
 #pragma unroll 1
     for (int c0 = 0; c0 < 256; c0 += 32) {
