@@ -14,26 +14,28 @@
 //   PV   : O_c[128 rows x 256]   += P[128 x 64] . V[64 x cols_c(256)] (M=128, N=256)
 // where each CTA's 256 V columns are exactly the first four 64-column chunks it
 // already holds.  The two partial S_c are summed across the pair through
-// distributed shared memory: CTA c owns the softmax of 64 rows (CTA 0 rows 0-63,
-// CTA 1 rows 64-127), receives the peer's partial for those rows, computes P,
-// and writes its P rows into both CTAs' P buffers.
+// distributed shared memory, split by tokens: CTA c owns the softmax of tokens
+// [32c, 32c+32) of every page for all 128 rows, receives the peer's partial for
+// that half, computes P for it, and writes it into both CTAs' P buffers.  Every
+// transfer between the pair is st.async with transaction-count completion on the
+// receiver's mbarrier (lowest latency, no bulk-copy engine work).
 //
-// Warp roles (192 threads; 320 for an FP8 cache):
+// Warp roles (224 threads; 352 for an FP8 cache):
 //   warp 0     TMA producer: Q once, then per page a block-table lookup and the
 //              CTA's 4 or 5 64x64 boxes (128B swizzle) into a 4-stage ring; L2
 //              prefetch of upcoming pages; owns the TMEM allocation.
-//   warp 1     MMA issuer (one thread).
+//   warp 1     QK^T issuer (one thread).
 //   warps 2-5  softmax / exchange / epilogue warpgroup.  Warp w reads TMEM lane
-//              quadrant w%4 (rows 32*(w%4) .. +31).  Quadrants of rows this CTA
-//              owns compute the softmax; the other two send their S partial rows
-//              to the peer.  Online softmax in the exp2 domain with a lazily
-//              updated reference max: O is rescaled only when a row's max grows
-//              by more than 2^8, coordinated across the pair by a per-page flag.
+//              quadrant w%4 (rows 32*(w%4) .. +31) and works on its CTA's token
+//              half of those rows.  Online softmax in the exp2 domain with lazily
+//              raised whole-number reference maxima, agreed between the pair one
+//              page behind (see the warpgroup's comment).
 //   warps 6-9  (FP8 cache) converter: the CTA's e4m3 columns land in the upper
 //              half of a stage; every thread first pulls its share into
 //              registers, then writes exact bf16 values (e4m3 is a subset of
 //              bf16) in the swizzled layout.  The per-tensor scale is folded into
 //              the softmax scale and the epilogue.
+//   warp 6/10  PV issuer (one thread; warp 10 with an FP8 cache).
 //
 // Q's c_kv columns are kept in tensor memory as the A operand of QK^T (read every
 // page; from TMEM they cost no shared-memory bandwidth and leave room for 4 page
@@ -57,14 +59,16 @@ constexpr int kQChunkBytes = 128 * 128;  // 128 rows x 128 B
 constexpr int kKvChunkBytes = 64 * 128;  // 64 tokens x 128 B
 constexpr int kStageBytes = kMaxCh * kKvChunkBytes;
 constexpr int kStages = 4;
-constexpr int kSinBytes = 64 * 64 * 4;  // peer's partial S for the 64 owned rows
+constexpr int kSinQuadBytes = 32 * 32 * 4;    // peer's partial S: 32 rows x 32 tokens of one quadrant
+constexpr int kSinBytes = 4 * kSinQuadBytes;
 constexpr int kPBytes = kRows * 128;    // P[128 rows x 64 tokens] bf16
 constexpr int kStageOff = 0;
 constexpr int kQStageOff = kStageOff + 2 * kStageBytes;  // Q's c_kv chunks land in stages 2-3, then go to TMEM
 static_assert(4 * kQChunkBytes <= 2 * kStageBytes, "Q staging");
-constexpr int kSinOff = kStageOff + kStages * kStageBytes;  // one S_in buffer
-constexpr int kPOff = kSinOff + kSinBytes;                    // two P buffers
-constexpr int kQpeOff = kPOff + 2 * kPBytes;                  // CTA 1's q_pe chunk (A from shared memory)
+constexpr int kSinOff = kStageOff + kStages * kStageBytes;  // S_in: the peer's partial scores, per quadrant
+constexpr int kSoutOff = kSinOff + kSinBytes;                 // S_out: partial scores staged for the peer
+constexpr int kPOff = kSoutOff + kSinBytes;                   // one P buffer
+constexpr int kQpeOff = kPOff + kPBytes;                      // CTA 1's q_pe chunk (A from shared memory)
 constexpr int kCtlOff = kQpeOff + kQChunkBytes;
 constexpr int kCtlBytes = 2048;
 constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;  // + alignment slack
@@ -77,7 +81,11 @@ constexpr uint32_t kColS = 256;  // S: two 64-column buffers
 constexpr uint32_t kColQ = 384;  // Q's c_kv chunks as the A operand: 2 bf16 per column, 128 columns
 
 constexpr int kSoftmaxWarp0 = 2;
-constexpr int kConvWarp0 = 6;
+constexpr int kConvWarp0 = 6;    // FP8 converter warps 6-9
+template <bool kFp8>
+__host__ __device__ constexpr int pv_warp() { return kFp8 ? 10 : 6; }
+template <bool kFp8>
+__host__ __device__ constexpr int block_threads() { return 32 * (pv_warp<kFp8>() + 1); }
 constexpr int kRawOff = kStageBytes / 2;  // e4m3 columns of a page in the upper half of a stage
 constexpr int kRawBox = 64 * 64;          // one 64 tokens x 64 bytes box
 
@@ -90,16 +98,9 @@ constexpr int kPrefetchPages = 4;
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
 
-// Per page and owner warp: each row's O rescale factor and whether any row of
-// the warp moved its reference max (flag = page + 1).  Copied to the peer with
-// the warp's 32 P rows.
-struct alignas(16) Meta {
-  float fac[32];
-  int flag;
-  int pad[3];
-};
-constexpr int kMetaBytes = sizeof(Meta);
-constexpr uint32_t kPvReadyTx = 2 * (32 * 128 + kMetaBytes);  // the peer's 2 owner warps' copies
+// Bytes the peer's warp of a quadrant delivers into pv_ready per page: its 32
+// rows' P halves (64 B each) and the references they were computed with.
+constexpr uint32_t kPvReadyTx = 32 * (64 + 4);
 
 struct Ctl {
   uint64_t q_full;
@@ -109,19 +110,18 @@ struct Ctl {
   uint64_t q_tmem;             // Q moved from shared to tensor memory (count 4)
   uint64_t s_full[2];          // QK^T of the page is in TMEM
   uint64_t s_free[2];          // the 4 softmax warps have read it (count 4)
-  uint64_t sin_full;           // peer's partial S landed (count 1 + 16 KB of st.async bytes)
-  uint64_t sin_free;           // peer's 2 owner warps consumed what this CTA sent (count 2, remote)
-  uint64_t p_free[2];          // PV of the buffer's previous page done in both CTAs (count 2)
-  uint64_t pv_ready[2];        // local owners wrote P (count 2) + the peer's P and meta copies landed
-  uint64_t rescaled[2];        // the 4 local warps rescaled O (count 4)
-  uint64_t fin;                // 1/l of all 128 rows delivered (count 4)
+  uint64_t sin_full[4];        // per quadrant: the peer's partial S landed (count 1 + 4 KB of st.async bytes)
+  uint64_t sin_free[4];        // per quadrant: the peer consumed what this CTA sent (count 1, remote)
+  uint64_t p_free;             // PV of the previous page done in both CTAs: P rewritable (count 2)
+  uint64_t pv_ready[2];        // local P halves written (count 4) + the peer's halves and references landed
+  uint64_t checked[2];         // the 4 local warps ran the page's reference check (count 4)
+  uint64_t fin;                // the peer's row sums delivered (count 4 + 512 B)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int poisoned;
-  Meta meta_local[2][2];       // [page buffer][owner warp]: written by this CTA's owners
-  Meta meta_peer[2][2];        // the same, copied in from the peer
-  float inv_l[kRows];
+  float u_peer[2][kRows];      // [P buffer][row]: reference the peer computed its half with
+  float l_peer[kRows];         // the peer's exp sums at the end
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
@@ -192,7 +192,7 @@ __device__ __forceinline__ bool wait_bar(Ctl* c, uint64_t* bar, uint32_t parity,
 }
 
 template <bool kFp8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(), 1)
     split_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
                        const __grid_constant__ CUtensorMap tm_kv, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -202,8 +202,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
   uint8_t* sKV = smem + kStageOff;
   uint8_t* sSin = smem + kSinOff;
   uint8_t* sQpe = smem + kQpeOff;
+  uint8_t* sSout = smem + kSoutOff;
   uint8_t* sP = smem + kPOff;
 
+  constexpr int kPvWarp = pv_warp<kFp8>();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t cta = cluster_ctarank();  // 0 or 1: which column half this CTA holds
@@ -236,16 +238,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
     mbar_init(&ctl->s_full[1], 1);
     mbar_init(&ctl->s_free[0], 4);
     mbar_init(&ctl->s_free[1], 4);
-    mbar_init(&ctl->sin_full, 1);
-    mbar_init(&ctl->sin_free, 2);
-    for (int e = 0; e < 2; ++e) {
-      mbar_init(&ctl->p_free[e], 2);
-      mbar_init(&ctl->pv_ready[e], 2);
-      mbar_init(&ctl->rescaled[e], 4);
-      for (int w = 0; w < 2; ++w) ctl->meta_local[e][w].flag = ctl->meta_peer[e][w].flag = 0;
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&ctl->sin_full[q], 1);
+      mbar_init(&ctl->sin_free[q], 1);
     }
+    for (int e = 0; e < 2; ++e) {
+      mbar_init(&ctl->pv_ready[e], 4);
+      mbar_init(&ctl->checked[e], 4);
+    }
+    mbar_init(&ctl->p_free, 2);
     mbar_init(&ctl->fin, 4);
-    mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->drain, 2);  // both MMA-issuing threads' last commits
     ctl->abort = 0;
     ctl->poisoned = len_ok ? 0 : 1;
     fence_mbarrier_init();
@@ -322,87 +325,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK^T issuer
+    // QK(j) as soon as page j has landed and its S buffer is free.  PV has a
+    // thread of its own (below), so a PV that becomes ready never waits behind
+    // the issue of a QK; the stage ring, S, S_in and P barriers bound how far QK
+    // runs ahead.
     if (lane == 0 && n_pages > 0) {
       const uint32_t kv_addr = smem_u32(sKV);
-      const uint32_t p_addr = smem_u32(sP);
       const uint64_t qpe_desc = sdesc_sw128(smem_u32(sQpe), 16, 1024);
-      int nres[2] = {0, 0};
       bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
-      // Greedy issue: QK(nq) as soon as its page has landed and S is free, PV(np)
-      // as soon as both CTAs' P(np) is in (and O rescaled, if flagged).  Polling
-      // with non-blocking tests keeps one pending PV from holding back the next
-      // page's QK.  The stage ring, S, S_in and P barriers bound how far QK runs
-      // ahead.
-      int nq = 0, np = 0;
-      int resc_state = 0;  // for page np: 0 = flags not read, 1 = no rescale, 2 = waiting for rescale
-      uint64_t t_last = globaltimer_ns();
-      while (ok && np < n_pages) {
-        bool progressed = false;
-        if (nq < n_pages && mbar_test_wait(smem_u32(&ctl->full[nq & 3]), (nq >> 2) & 1) &&
-            mbar_test_wait(smem_u32(&ctl->s_free[nq & 1]), ((nq >> 1) & 1) ^ 1)) {
-          tc_fence_after();
-          const uint64_t k_desc = sdesc_sw128(kv_addr + (nq & 3) * kStageBytes, 16, 1024);
-          const uint32_t d = tmem + kColS + (nq & 1) * 64;
-          for (int k = 0; k < 4; ++k) {
+      for (int j = 0; ok && j < n_pages; ++j) {
+        if (!wait_bar(ctl, &ctl->full[j & 3], (j >> 2) & 1, p, 3) ||
+            !wait_bar(ctl, &ctl->s_free[j & 1], ((j >> 1) & 1) ^ 1, p, 4))
+          break;
+        tc_fence_after();
+        const uint64_t k_desc = sdesc_sw128(kv_addr + (j & 3) * kStageBytes, 16, 1024);
+        const uint32_t d = tmem + kColS + (j & 1) * 64;
+        for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)  // A = Q chunk k from TMEM: 16 k per MMA = 8 columns
-              mma_bf16_ts(d, tmem + kColQ + k * 32 + kk * 8,
-                          k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4), kIdescQK, (k | kk) ? 1u : 0u);
-          }
-          if (nch == 5) {  // k_pe: A = q_pe from shared memory
+          for (int kk = 0; kk < 4; ++kk)  // A = Q chunk k from TMEM: 16 k per MMA = 8 columns
+            mma_bf16_ts(d, tmem + kColQ + k * 32 + kk * 8, k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4),
+                        kIdescQK, (k | kk) ? 1u : 0u);
+        }
+        if (nch == 5) {  // k_pe: A = q_pe from shared memory
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4),
-                          k_desc + (uint64_t)((4 * kKvChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
-          }
-          mma_commit(&ctl->s_full[nq & 1]);
-          ++nq;
-          progressed = true;
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4),
+                        k_desc + (uint64_t)((4 * kKvChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
         }
-        if (np < nq) {
-          const int e = np & 1;
-          if (resc_state == 0 && mbar_test_wait(smem_u32(&ctl->pv_ready[e]), (np >> 1) & 1)) {
-            const volatile Meta* ml = ctl->meta_local[e];
-            const volatile Meta* mp = ctl->meta_peer[e];
-            resc_state = (ml[0].flag == np + 1 || ml[1].flag == np + 1 || mp[0].flag == np + 1 ||
-                          mp[1].flag == np + 1) ? 2 : 1;  // some row's reference max moved
-          }
-          if (resc_state == 2 && mbar_test_wait(smem_u32(&ctl->rescaled[e]), nres[e] & 1)) {
-            ++nres[e];
-            resc_state = 1;
-          }
-          if (resc_state == 1) {
-            tc_fence_after();
-            const uint64_t v_desc = sdesc_sw128(kv_addr + (np & 3) * kStageBytes, kKvChunkBytes, 1024);
-            const uint64_t p_desc = sdesc_sw128(p_addr + e * kPBytes, 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ss(tmem + kColO, p_desc + (uint64_t)((kk * 32) >> 4), v_desc + (uint64_t)((kk * 2048) >> 4),
-                          kIdescPV, (np > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&ctl->empty[np & 3]);           // stage free; O current through page np
-            mma_commit_multicast(&ctl->p_free[e], 3);  // P buffer e reusable, in both CTAs
-            ++np;
-            resc_state = 0;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          t_last = globaltimer_ns();
-        } else if (*(volatile int*)&ctl->abort) {
-          ok = false;
-        } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
-          *(volatile int*)&ctl->abort = 1;
-          report_error(p.err, MLA_ERR_TIMEOUT, blockIdx.z, 3, blockIdx.y);
-          ok = false;
-        }
+        mma_commit(&ctl->s_full[j & 1]);
       }
       mma_commit(&ctl->drain);  // every MMA of this thread has completed before TMEM is freed
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(smem_u32(&ctl->drain), 0))
         if (globaltimer_ns() - t0 > kWaitLimitNs) break;
     }
-  } else if (kFp8 && warp >= kConvWarp0) {
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ PV issuer
+    // PV(j) once both CTAs' P halves of page j are in and the local warps have
+    // checked its references (and scaled O or P where they moved).
+    if (lane == 0 && n_pages > 0) {
+      const uint32_t kv_addr = smem_u32(sKV);
+      const uint32_t p_addr = smem_u32(sP);
+      for (int j = 0; j < n_pages; ++j) {
+        if (!wait_bar(ctl, &ctl->pv_ready[j & 1], (j >> 1) & 1, p, 5) ||
+            !wait_bar(ctl, &ctl->checked[j & 1], (j >> 1) & 1, p, 7))
+          break;
+        // The peer's P halves arrive by st.async, generic-proxy writes: the fence
+        // after the acquiring waits makes them visible to the MMA's operand reads.
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const uint64_t v_desc = sdesc_sw128(kv_addr + (j & 3) * kStageBytes, kKvChunkBytes, 1024);
+        const uint64_t p_desc = sdesc_sw128(p_addr, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(tmem + kColO, p_desc + (uint64_t)((kk * 32) >> 4), v_desc + (uint64_t)((kk * 2048) >> 4),
+                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&ctl->empty[j & 3]);      // stage free; O current through page j
+        mma_commit_multicast(&ctl->p_free, 3);  // P reusable, in both CTAs
+      }
+      mma_commit(&ctl->drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(smem_u32(&ctl->drain), 0))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  } else if (kFp8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
     // ------------------------------------------------------------ e4m3 -> bf16 converter
     const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
     const int units = nch * 64;                    // (chunk, token) pairs of 64 bytes
@@ -447,61 +434,141 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
     }
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
     // ------------------------------------------------------------ softmax / exchange warpgroup
+    // Each CTA owns one half of every page's 64 tokens (CTA c: tokens 32c..32c+31)
+    // for all 128 rows; warp w handles the rows of TMEM lane quadrant w%4.  Per
+    // page a warp hands the peer the partial scores of the peer's token half,
+    // adds the peer's partial for its own half, and computes P for its half, which
+    // it writes into both CTAs' P buffers.
+    //
+    // Reference maxima.  P of one row must share one reference across both
+    // halves, yet neither CTA sees the other's scores.  Each CTA computes with
+    // its own reference r_ref (a whole number in the exp2 domain, so that any two
+    // differ by a power of two), raised lazily to ceil(max) when a score exceeds
+    // it by more than 2^8.  With every P half goes the reference it used; once
+    // both halves of page k are in, each CTA takes the larger of the two and of
+    // the previous agreed value, scales O if the agreed value moved, and scales
+    // any P half computed against a lower reference (a raise, or a reference the
+    // CTA had not yet learnt from its peer) before PV(k).  Outside of raises,
+    // which occur on a split's first pages and when a row's max jumps, that check
+    // touches nothing.
     const int quad = warp & 3;
     const int r = quad * 32 + lane;              // row within the group (TMEM lane)
-    const bool owner = (quad >> 1) == (int)cta;  // CTA 0 owns rows 0-63, CTA 1 rows 64-127
-    const int ri = r & 63;                       // row index within the owned / sent half
     const bool row_ok = row0 + r < p.rows;
     const int qi = (row0 + r) / p.num_heads;
     const int vis = L - p.q_len + 1 + qi;        // tokens this row may see
     const float sc2 = p.softmax_scale * kv_scale * kLog2e;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t sin_local = smem_u32(sSin);
-    const uint32_t sin_peer = mapa_shared(sin_local, peer);
+    const uint32_t col_own = kColS + 32 * cta;    // S columns of this CTA's token half (within a buffer)
+    const uint32_t col_oth = kColS + 32 * peer;
+    uint8_t* sin_row = sSin + quad * kSinQuadBytes + lane * 128;  // 32 fp32 of the peer's partial
+    uint8_t* sout_quad = sSout + quad * kSinQuadBytes;
+    uint8_t* sout_row = sout_quad + lane * 128;
+    const uint32_t sin_quad_peer = mapa_shared(smem_u32(sSin + quad * kSinQuadBytes), peer);
+    const uint32_t sin_full_peer = mapa_shared(smem_u32(&ctl->sin_full[quad]), peer);
+    const uint32_t sin_free_peer = mapa_shared(smem_u32(&ctl->sin_free[quad]), peer);
     const uint32_t p_peer = mapa_shared(smem_u32(sP), peer);
-    const int ow = quad & 1;  // owner-warp index of this quadrant (CTA 0: quads 0,1; CTA 1: quads 2,3)
-    float m_ref = -INFINITY, l_sum = 0.f;
+    float r_ref = -INFINITY;   // reference this CTA computes P with
+    float a_ref = -INFINITY;   // reference both CTAs agreed on, through the last checked page
+    float l_sum = 0.f;         // exp sum over this CTA's token halves, relative to r_ref
+    float u_prev = -INFINITY;  // reference the previous page was computed with
     bool poisoned = !len_ok;
     bool ok = true;
 
-    // Every warp runs this loop on its own: decisions after a bounded wait are
-    // made warp-uniform (__all_sync), and no named barrier sits inside the loop,
-    // so sender warps run a page ahead of the owners and a warp that gives up
-    // cannot strand the others on a barrier.
-    //
-    // Rescale check for page jj, run at the start of iteration jj+2 (by then both
-    // CTAs' P(jj) has long been written, so the wait is free): if any row of either
-    // CTA moved its reference max on page jj, each warp rescales its lanes (rows)
-    // of O by fac before PV(jj) is issued.  It precedes the wait for S(jj+2):
-    // PV(jj) is issued before QK(jj+2), so waiting for S first could deadlock.
-    auto rescale_check = [&](int jj) -> bool {
-      const int e = jj & 1;
-      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->pv_ready[e], (jj >> 1) & 1, p, 11))) return false;
-      const volatile Meta* ml = ctl->meta_local[e];
-      const volatile Meta* mp = ctl->meta_peer[e];
-      const bool resc = ml[0].flag == jj + 1 || ml[1].flag == jj + 1 || mp[0].flag == jj + 1 || mp[1].flag == jj + 1;
-      if (!resc) return true;
-      // O holds pages < jj once PV(jj-1) has completed (its commit covers all before).
-      if (jj > 0 &&
-          !__all_sync(0xffffffffu, wait_bar(ctl, &ctl->empty[(jj - 1) & 3], ((jj - 1) >> 2) & 1, p, 12)))
-        return false;
+    // 16-byte chunk u (0..7, before the swizzle) of this thread's row of P buffer e.
+    auto p_chunk = [&](int u) -> uint8_t* { return sP + r * 128 + ((u ^ (r & 7)) << 4); };
+
+    // S(jj) from TMEM: this CTA's token half stays in `own`; the peer's half is
+    // staged in S_out and goes to the peer's S_in for this quadrant as one 4 KB
+    // bulk copy, once the peer has consumed the previous page's (which also means
+    // the previous copy has read S_out).  The copy engine carries the bytes, so
+    // the warp does not stall on the pair's link.
+    auto take_s = [&](int jj, float (&own)[32]) -> bool {
+      const int sb = jj & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[sb], (jj >> 1) & 1, p, 6))) return false;
       tc_fence_after();
-      __syncwarp();
-      const float f = owner ? ctl->meta_local[e][ow].fac[lane] : ctl->meta_peer[e][ow].fac[lane];
-#pragma unroll 1
-      for (int g = 0; g < 16; ++g) {
-        uint32_t v[16];
-        const uint32_t ta = tmem + lane_base + kColO + g * 16;
-        tmem_ld16(ta, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
-        tmem_st16(ta, v);
-      }
-      tmem_st_wait();
+      uint32_t mine[2][16], oth[2][16];
+      tmem_ld16(tmem + lane_base + col_own + sb * 64, mine[0]);
+      tmem_ld16(tmem + lane_base + col_own + sb * 64 + 16, mine[1]);
+      tmem_ld16(tmem + lane_base + col_oth + sb * 64, oth[0]);
+      tmem_ld16(tmem + lane_base + col_oth + sb * 64 + 16, oth[1]);
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->rescaled[e]);
+      if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) own[k] = __uint_as_float(mine[k >> 4][k & 15]);
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_free[quad], (jj & 1) ^ 1, p, 13))) return false;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(sout_row + ((u ^ (lane & 7)) << 4)) =
+            make_uint4(oth[u >> 2][(u & 3) * 4], oth[u >> 2][(u & 3) * 4 + 1], oth[u >> 2][(u & 3) * 4 + 2],
+                       oth[u >> 2][(u & 3) * 4 + 3]);
+      fence_proxy_async_smem();  // staged rows visible to the copy engine
+      __syncwarp();
+      if (lane == 0) bulk_copy_to_peer(sin_quad_peer, sout_quad, kSinQuadBytes, sin_full_peer);
+      return true;
+    };
+
+    // Page k's reference check, run once both CTAs' P(k) and references are in
+    // and before PV(k) may be issued (the MMA waits for `checked`).
+    auto check = [&](int k, float u_own) -> bool {
+      const int e = k & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->pv_ready[e], (k >> 1) & 1, p, 11))) return false;
+      const float u_oth = ctl->u_peer[e][r];
+      const float an = fmaxf(a_ref, fmaxf(u_own, u_oth));
+      const bool resc = k > 0 && an > a_ref;  // PV(0) overwrites O
+      const bool fix_own = u_own < an, fix_oth = u_oth < an;
+      if (__any_sync(0xffffffffu, resc || fix_own || fix_oth)) {
+        if (__any_sync(0xffffffffu, resc)) {
+          // O holds exactly pages < k once PV(k-1) has completed.
+          if (!__all_sync(0xffffffffu,
+                          wait_bar(ctl, &ctl->empty[(k - 1) & 3], ((k - 1) >> 2) & 1, p, 12)))
+            return false;
+          tc_fence_after();
+          const float f = resc ? ex2(a_ref - an) : 1.f;
+#pragma unroll 1
+          for (int g = 0; g < 16; ++g) {
+            uint32_t v[16];
+            const uint32_t ta = tmem + lane_base + kColO + g * 16;
+            tmem_ld16(ta, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+            tmem_st16(ta, v);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+        }
+        // P halves computed against a lower reference; the factors are powers of two.
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const bool fix = h == (int)cta ? fix_own : fix_oth;
+          if (fix) {
+            const float f = ex2((h == (int)cta ? u_own : u_oth) - an);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4* c = reinterpret_cast<uint4*>(p_chunk(4 * h + u));
+              uint4 w = *c;
+              uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[i]));
+                __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
+                wv[i] = *reinterpret_cast<uint32_t*>(&y);
+              }
+              *c = w;
+            }
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      if (an > r_ref) {
+        l_sum *= ex2(r_ref - an);
+        r_ref = an;
+      }
+      a_ref = an;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->checked[e]);
       return true;
     };
 
@@ -534,69 +601,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
 
     // Block-table entries are loaded one page ahead: a global load consumed in
     // the same iteration would stall every page for a full memory latency.
-    int page_next = (n_pages > 0 && owner) ? bt_row[0] : 0;
+    int page_next = n_pages > 0 ? bt_row[0] : 0;
+    float sv_next[32];
+    if (ok && n_pages > 0 && !take_s(0, sv_next)) ok = false;
     for (int j = 0; ok && j < n_pages; ++j) {
-      const int s = j & 1;   // exchange buffers (S_in, P, meta)
-      const int st = j & 3;  // page stage
+      const int e = j & 1;   // pv_ready / checked / peer references of this page
       const int tok0 = lo + j * kPage;  // lo is page aligned
       const int page = page_next;
-      if (owner && j + 1 < n_pages) page_next = bt_row[j + 1];
-      const bool page_ok = !owner || (page >= 0 && page < p.num_pages);  // only owners use it
+      if (j + 1 < n_pages) page_next = bt_row[j + 1];
+      const bool page_ok = page >= 0 && page < p.num_pages;
       poisoned |= !page_ok;
-      if (j >= 2 && !rescale_check(j - 2)) { ok = false; break; }
-      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[s], (j >> 1) & 1, p, 6))) { ok = false; break; }
-      tc_fence_after();
-      float sv[64];
-      {
-        uint32_t raw[4][16];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) tmem_ld16(tmem + lane_base + kColS + s * 64 + g * 16, raw[g]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-#pragma unroll
-          for (int k = 0; k < 16; ++k) sv[g * 16 + k] = __uint_as_float(raw[g][k]);
+      // The previous page's references first: PV(j-1), and with it the release
+      // of its stage for the next page load, waits for this check.
+      if (j >= 1 && !check(j - 1, u_prev)) {
+        ok = false;
+        break;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->s_free[s]);
-
-      if (!owner) {
-        // ---- sender: partial S of a row the peer owns -> peer's S_in[s][ri]
-        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_free, (j & 1) ^ 1, p, 13))) {
-          ok = false;
-          break;
-        }
-        const uint32_t dst = sin_peer + ri * 256;
-        const uint32_t bar = mapa_shared(smem_u32(&ctl->sin_full), peer);
+      float sv[32];
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          st_async_v4(dst + ((u ^ (ri & 7)) << 4),
-                      make_uint4(__float_as_uint(sv[4 * u]), __float_as_uint(sv[4 * u + 1]),
-                                 __float_as_uint(sv[4 * u + 2]), __float_as_uint(sv[4 * u + 3])),
-                      bar);
-      } else {
-        // ---- owner: add the peer's partial, softmax, P into both CTAs
-        // The peer's two sender warps deliver 16 KB of st.async bytes per page.
-        if (ow == 0 && lane == 0) mbar_arrive_expect_tx(&ctl->sin_full, kSinBytes);
-        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_full, j & 1, p, 14))) {
-          ok = false;
-          break;
-        }
-        // Full score = own partial + the peer's partial.  Pages that every row of
-        // the warp sees in full (all but a split's last page, normally) take a
-        // fast path: add and max on raw scores (the scale is positive, so max
-        // commutes with it), then p = 2^(s*scale - m) in one FMA + ex2.  Other
-        // pages mask and scale first; masked columns, possibly NaN garbage, become
-        // -inf and then exactly 0.
-        const float4* src = reinterpret_cast<const float4*>(sSin + ri * 256);
-        const int n_vis = (page_ok && row_ok) ? min(max(vis - tok0, 0), kPage) : 0;
-        const bool fast = __all_sync(0xffffffffu, n_vis == kPage);
-        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      for (int k = 0; k < 32; ++k) sv[k] = sv_next[k];
+
+      // The peer's partial of this CTA's token half.  Pages that every row of the
+      // warp sees in full (all but a split's last page, normally) take a fast
+      // path: add and max on raw scores (the scale is positive, so max commutes
+      // with it), then p = 2^(s*scale - ref) in one FMA + ex2.  Other pages mask
+      // and scale first; masked columns, possibly NaN garbage, become -inf and
+      // then exactly 0.
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->sin_full[quad], kSinQuadBytes);
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_full[quad], j & 1, p, 14))) {
+        ok = false;
+        break;
+      }
+      const int tok_c = tok0 + 32 * (int)cta;
+      const int n_vis = (page_ok && row_ok) ? min(max(vis - tok_c, 0), 32) : 0;
+      const bool fast = __all_sync(0xffffffffu, n_vis == 32);
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      {
+        const float4* src = reinterpret_cast<const float4*>(sin_row);
         if (fast) {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const float4 v = src[u ^ (ri & 7)];
+          for (int u = 0; u < 8; ++u) {
+            const float4 v = src[u ^ (lane & 7)];
             sv[4 * u] += v.x;
             sv[4 * u + 1] += v.y;
             sv[4 * u + 2] += v.z;
@@ -606,8 +651,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
           }
         } else {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const float4 v = src[u ^ (ri & 7)];
+          for (int u = 0; u < 8; ++u) {
+            const float4 v = src[u ^ (lane & 7)];
             const float a[4] = {sv[4 * u] + v.x, sv[4 * u + 1] + v.y, sv[4 * u + 2] + v.z, sv[4 * u + 3] + v.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -617,134 +662,127 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
             }
           }
         }
-        float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-        if (fast) mx *= sc2;
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&ctl->sin_free), peer));
+      }
+      float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      if (fast) mx *= sc2;
+      __syncwarp();  // every lane's S_in values are in registers
+      if (lane == 0) mbar_arrive_cluster_relaxed(sin_free_peer);
 
-        // V rows of tokens at or past L (or of a page that was never loaded) may
-        // hold anything, NaN included; zero this CTA's 256 V columns of them.
-        const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
-        if (ri >= n_valid) {
-          uint8_t* stage = sKV + st * kStageBytes;
+      // Next page's scores to the peer while this page's P is computed.
+      if (j + 1 < n_pages && !take_s(j + 1, sv_next)) {
+        ok = false;
+        break;
+      }
+
+      // V rows of tokens at or past L (or of a page that was never loaded) may
+      // hold anything, NaN included; zero this CTA's 256 V columns of them.
+      // Thread t of the group clears half of token row t/2.
+      const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
+      if (n_valid < kPage) {
+        const int t = r >> 1;
+        if (t >= n_valid) {
+          uint8_t* stage = sKV + (j & 3) * kStageBytes;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint4* rowp = reinterpret_cast<uint4*>(stage + c * kKvChunkBytes + ri * 128);
+          for (int c = 0; c < 2; ++c) {
+            uint4* rowp = reinterpret_cast<uint4*>(stage + ((r & 1) * 2 + c) * kKvChunkBytes + t * 128);
 #pragma unroll
             for (int u = 0; u < 8; ++u) rowp[u] = make_uint4(0, 0, 0, 0);
           }
         }
+      }
 
-        const bool need = row_ok && (mx > m_ref + kRescaleThreshold);
-        float fac = 1.f;
-        if (need) {
-          fac = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mx);
-          l_sum *= fac;
-          m_ref = mx;
-        }
-        uint4 pk[8];
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
-        if (fast) {
-          const float nm = -m_ref;
+      if (mx > r_ref + kRescaleThreshold) {  // false while every column is masked
+        const float u = ceilf(mx);
+        l_sum *= ex2(r_ref - u);
+        r_ref = u;
+      }
+      const float u_cur = r_ref;
+      uint4 pk[4];
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      if (fast) {
+        const float nm = -r_ref;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint32_t w[4];
+        for (int u = 0; u < 4; ++u) {
+          uint32_t w[4];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const float p0 = ex2(fmaf(sv[u * 8 + 2 * h], sc2, nm));
-              const float p1 = ex2(fmaf(sv[u * 8 + 2 * h + 1], sc2, nm));
-              part[h] += p0 + p1;
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-              w[h] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int h = 0; h < 4; ++h) {
+            const float p0 = ex2(fmaf(sv[u * 8 + 2 * h], sc2, nm));
+            const float p1 = ex2(fmaf(sv[u * 8 + 2 * h + 1], sc2, nm));
+            part[h] += p0 + p1;
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            w[h] = *reinterpret_cast<uint32_t*>(&b2);
           }
-        } else {
+          pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint32_t w[4];
+        for (int u = 0; u < 4; ++u) {
+          uint32_t w[4];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
-              const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - m_ref);
-              const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - m_ref);
-              part[h] += p0 + p1;
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-              w[h] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int h = 0; h < 4; ++h) {
+            const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
+            const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - r_ref);
+            const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - r_ref);
+            part[h] += p0 + p1;
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            w[h] = *reinterpret_cast<uint32_t*>(&b2);
           }
-        }
-        l_sum += (part[0] + part[1]) + (part[2] + part[3]);
-        // Both CTAs' PV of page j-2 must be done before P buffer s is rewritten.
-        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->p_free[s], ((j >> 1) & 1) ^ 1, p, 15))) {
-          ok = false;
-          break;
-        }
-        const uint32_t off = s * kPBytes + r * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(sP + off + ((u ^ (r & 7)) << 4)) = pk[u];
-        Meta& me = ctl->meta_local[s][ow];
-        me.fac[lane] = fac;
-        const bool any_need = __any_sync(0xffffffffu, need) && j > 0;  // page 0's PV overwrites O
-        if (lane == 0) me.flag = any_need ? j + 1 : 0;
-        fence_proxy_async_smem();  // P rows and meta visible to the MMA and the bulk copy engine
-        __syncwarp();
-        if (lane == 0) {
-          // This warp's 32 P rows (4 KB, contiguous) and its meta go to the peer
-          // through the async proxy; the peer's pv_ready counts the bytes.
-          const uint32_t bar = mapa_shared(smem_u32(&ctl->pv_ready[s]), peer);
-          const uint32_t rows_off = s * kPBytes + quad * 32 * 128;
-          bulk_copy_to_peer(p_peer + rows_off, sP + rows_off, 32 * 128, bar);
-          bulk_copy_to_peer(mapa_shared(smem_u32(&ctl->meta_peer[s][ow]), peer), &me, kMetaBytes, bar);
-          if (ow == 0)
-            mbar_arrive_expect_tx(&ctl->pv_ready[s], kPvReadyTx);
-          else
-            mbar_arrive(&ctl->pv_ready[s]);
+          pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
+      l_sum += (part[0] + part[1]) + (part[2] + part[3]);
+
+      // Both CTAs' PV of page j-1 must be done before P is rewritten.
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->p_free, (j & 1) ^ 1, p, 15))) {
+        ok = false;
+        break;
+      }
+      const uint32_t pv_bar_peer = mapa_shared(smem_u32(&ctl->pv_ready[e]), peer);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint8_t* c = p_chunk(4 * (int)cta + u);
+        *reinterpret_cast<uint4*>(c) = pk[u];
+        st_async_v4(p_peer + (uint32_t)(c - sP), pk[u], pv_bar_peer);
+      }
+      st_async_u32(mapa_shared(smem_u32(&ctl->u_peer[e][r]), peer), __float_as_uint(u_cur), pv_bar_peer);
+      fence_proxy_async_smem();  // local P rows (and any zeroed V rows) visible to the MMA
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->pv_ready[e], kPvReadyTx);
+      u_prev = u_cur;
     }
-    if (ok && n_pages >= 2 && !rescale_check(n_pages - 2)) ok = false;
-    if (ok && n_pages >= 1 && !rescale_check(n_pages - 1)) ok = false;
+    if (ok && n_pages >= 1 && !check(n_pages - 1, u_prev)) ok = false;
     ok = !wg_sync_or(!ok);  // the epilogue decides as one group
 
     // ------------------------------------------------------------ epilogue
-    if (owner) {
-      const bool has = l_sum > 0.f;
-      const float il = has ? kv_scale / l_sum : 0.f;
-      ctl->inv_l[r] = il;
-      st_cluster_u32(mapa_shared(smem_u32(&ctl->inv_l[r]), peer), __float_as_uint(il));
-      const int64_t grow = (int64_t)b * p.rows + row0 + r;
-      if (row_ok) {
-        float lv = has ? (m_ref + lg2(l_sum)) * kLn2 : -INFINITY;
-        if (poisoned || !ok) lv = NAN;
-        if (p.splits == 1) {
-          if (p.lse) p.lse[grow] = lv;
-        } else {
-          p.partials[(grow * p.splits + split) * kPartRow + kKvLora] = lv;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->fin), cta));
-        mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->fin), peer));
-      }
-    }
+    // Row sums of both token halves: every row's partial goes to the peer.
+    st_async_u32(mapa_shared(smem_u32(&ctl->l_peer[r]), peer), __float_as_uint(l_sum),
+                 mapa_shared(smem_u32(&ctl->fin), peer));
+    if (lane == 0) mbar_arrive_expect_tx(&ctl->fin, 32 * 4);
     if (poisoned) atomicOr(&ctl->poisoned, 1);
-    bool fail = !wait_bar<true>(ctl, &ctl->fin, 0, p, 16);
+    bool fail = !wait_bar(ctl, &ctl->fin, 0, p, 16);
     fail |= !ok || (n_pages > 0 && !wait_bar(ctl, &ctl->empty[(n_pages - 1) & 3], ((n_pages - 1) >> 2) & 1, p, 8));
     fail = wg_sync_or(fail);
     tc_fence_after();
     __syncwarp();
     const bool have_o = !fail && n_pages > 0;
     const bool bad = ctl->poisoned != 0 || fail;
-    const int rows_here = min(kRows, p.rows - row0);
+    const float l_tot = l_sum + ctl->l_peer[r];
+    const bool has = l_tot > 0.f;
+    const float il = has ? kv_scale / l_tot : 0.f;
     const int64_t grow0 = (int64_t)b * p.rows + row0;
+    if (cta == 0 && row_ok) {
+      const float lv = bad ? NAN : (has ? (r_ref + lg2(l_tot)) * kLn2 : -INFINITY);
+      if (p.splits == 1) {
+        if (p.lse) p.lse[grow0 + r] = lv;
+      } else {
+        p.partials[((grow0 + r) * p.splits + split) * kPartRow + kKvLora] = lv;
+      }
+    }
+    const int rows_here = min(kRows, p.rows - row0);
     // O_c rows are TMEM lanes: stage 32 rows x 32 columns through shared memory
-    // (the P buffers, idle once the last PV has completed) so global stores run
+    // (S_out and P, idle once the last PV has completed) so global stores run
     // along the 512 columns.
-    float* tile = reinterpret_cast<float*>(sP) + (warp - kSoftmaxWarp0) * (32 * 33);
-    const float il = ctl->inv_l[r];
+    float* tile = reinterpret_cast<float*>(sSout) + (warp - kSoftmaxWarp0) * (32 * 33);
 #pragma unroll 1
     for (int c0 = 0; c0 < 256; c0 += 32) {
       uint32_t v[2][16];
@@ -776,7 +814,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? 320 : 192, 1)
     }
     tc_fence_before();
   }
-
   __syncthreads();
   cluster_sync_all();  // no remote store or arrive can target a CTA that has exited
   if (warp == 0) {
@@ -836,12 +873,12 @@ cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
     auto kern = split_kv_tc_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 320, kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, p);
+    kern<<<grid, block_threads<true>(), kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, p);
   } else {
     auto kern = split_kv_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 192, kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, p);
+    kern<<<grid, block_threads<false>(), kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, p);
   }
   return cudaGetLastError();
 }

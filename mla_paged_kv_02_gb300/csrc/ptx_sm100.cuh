@@ -110,6 +110,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint4 v, uint
                : "memory");
 }
 
+// The same for one 32-bit word (4 transaction bytes).
+__device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t v, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr),
+               "r"(v), "r"(cluster_bar)
+               : "memory");
+}
+
 // Bulk copy of this CTA's shared memory into a peer CTA's, completing `bytes`
 // transaction bytes on the peer's mbarrier (async proxy end to end).
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void* src, uint32_t bytes,
