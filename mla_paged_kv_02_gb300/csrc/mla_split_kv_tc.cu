@@ -94,6 +94,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far above any legitimate wait
 constexpr int kPrefetchPages = 4;
+constexpr int kCheckPos = 1;  // where in a page's iteration the previous page is checked
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
@@ -611,9 +612,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       if (j + 1 < n_pages) page_next = bt_row[j + 1];
       const bool page_ok = page >= 0 && page < p.num_pages;
       poisoned |= !page_ok;
-      // The previous page's references first: PV(j-1), and with it the release
-      // of its stage for the next page load, waits for this check.
-      if (j >= 1 && !check(j - 1, u_prev)) {
+      // The previous page's references are checked before this page's reference
+      // is settled; PV(j-1), and with it the release of its stage, waits for it.
+      if (kCheckPos == 0 && j >= 1 && !check(j - 1, u_prev)) {
         ok = false;
         break;
       }
@@ -668,8 +669,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       __syncwarp();  // every lane's S_in values are in registers
       if (lane == 0) mbar_arrive_cluster_relaxed(sin_free_peer);
 
+      if (kCheckPos == 1 && j >= 1 && !check(j - 1, u_prev)) {
+        ok = false;
+        break;
+      }
+
       // Next page's scores to the peer while this page's P is computed.
       if (j + 1 < n_pages && !take_s(j + 1, sv_next)) {
+        ok = false;
+        break;
+      }
+
+      if (kCheckPos == 2 && j >= 1 && !check(j - 1, u_prev)) {
         ok = false;
         break;
       }
@@ -737,17 +748,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         ok = false;
         break;
       }
-      const uint32_t pv_bar_peer = mapa_shared(smem_u32(&ctl->pv_ready[e]), peer);
+      // Local rows first, fenced and signalled before the remote copies are
+      // issued, so that the fence does not wait on stores queued for the link.
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint8_t* c = p_chunk(4 * (int)cta + u);
-        *reinterpret_cast<uint4*>(c) = pk[u];
-        st_async_v4(p_peer + (uint32_t)(c - sP), pk[u], pv_bar_peer);
-      }
-      st_async_u32(mapa_shared(smem_u32(&ctl->u_peer[e][r]), peer), __float_as_uint(u_cur), pv_bar_peer);
+      for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(p_chunk(4 * (int)cta + u)) = pk[u];
       fence_proxy_async_smem();  // local P rows (and any zeroed V rows) visible to the MMA
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&ctl->pv_ready[e], kPvReadyTx);
+      const uint32_t pv_bar_peer = mapa_shared(smem_u32(&ctl->pv_ready[e]), peer);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        st_async_v4(p_peer + (uint32_t)(p_chunk(4 * (int)cta + u) - sP), pk[u], pv_bar_peer);
+      st_async_u32(mapa_shared(smem_u32(&ctl->u_peer[e][r]), peer), __float_as_uint(u_cur), pv_bar_peer);
       u_prev = u_cur;
     }
     if (ok && n_pages >= 1 && !check(n_pages - 1, u_prev)) ok = false;
