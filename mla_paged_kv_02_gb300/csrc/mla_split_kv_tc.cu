@@ -22,8 +22,8 @@
 //
 // Warp roles (224 threads; 352 for an FP8 cache):
 //   warp 0     TMA producer: Q once, then per page a block-table lookup and the
-//              CTA's 4 or 5 64x64 boxes (128B swizzle) into a 4-stage ring; L2
-//              prefetch of upcoming pages; owns the TMEM allocation.
+//              CTA's 4 or 5 64x64 boxes (128B swizzle) into a 4-stage ring; owns
+//              the TMEM allocation.
 //   warp 1     QK^T issuer (one thread).
 //   warps 2-5  softmax / exchange / epilogue warpgroup.  Warp w reads TMEM lane
 //              quadrant w%4 (rows 32*(w%4) .. +31) and works on its CTA's token
@@ -93,7 +93,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far above any legitimate wait
-constexpr int kPrefetchPages = 4;
 constexpr int kCheckPos = 1;  // where in a page's iteration the previous page is checked
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
@@ -269,17 +268,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_pages > 0) {
       prefetch_tmap(&tm_kv);
-      const int64_t page_bytes = (int64_t)kPage * kRow * (kFp8 ? 1 : 2);
-      // A page is one contiguous block of the cache; CTA 0 pulls the next few
-      // whole pages into L2 so that freed stages refill at L2 latency.
-      auto prefetch_page = [&](int j) {
-        if (cta == 0 && j < n_pages) {
-          const int pg = bt_row[j];
-          if (pg >= 0 && pg < p.num_pages)
-            prefetch_l2(static_cast<const uint8_t*>(p.kv) + pg * page_bytes, (uint32_t)page_bytes);
-        }
-      };
-      for (int j = 0; j < kPrefetchPages; ++j) prefetch_page(j);
+      // No L2 prefetch of upcoming pages: it goes through the same copy engine
+      // as the pair's partial-score transfers and measured slower.
       const int qrow = b * p.rows + row0;
       mbar_arrive_expect_tx(&ctl->q_full, nch * kQChunkBytes);
       for (int k = 0; k < nch; ++k) {
@@ -295,12 +285,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         const int s = j & 3;
         const int page = next_page;
         if (j + 1 < n_pages) next_page = bt_row[j + 1];  // lookups ahead of the waits
-        const int pf = (cta == 0 && j + kPrefetchPages < n_pages) ? bt_row[j + kPrefetchPages] : -1;
         // Stages 2-3 hold Q until the softmax warps have moved it into TMEM.
         if (j == 2 && !wait_bar(ctl, &ctl->q_tmem, 0, p, 17)) break;
         if (!wait_bar(ctl, &ctl->empty[s], ((j >> 2) & 1) ^ 1, p, 1)) break;
-        if (pf >= 0 && pf < p.num_pages)
-          prefetch_l2(static_cast<const uint8_t*>(p.kv) + pf * page_bytes, (uint32_t)page_bytes);
         uint64_t* land = kFp8 ? &ctl->raw_full[s] : &ctl->full[s];
         uint8_t* stage = sKV + s * kStageBytes;
         if (page < 0 || page >= p.num_pages) {
