@@ -16,9 +16,11 @@
 // already holds.  The two partial S_c are summed across the pair through
 // distributed shared memory, split by tokens: CTA c owns the softmax of tokens
 // [32c, 32c+32) of every page for all 128 rows, receives the peer's partial for
-// that half, computes P for it, and writes it into both CTAs' P buffers.  Every
-// transfer between the pair is st.async with transaction-count completion on the
-// receiver's mbarrier (lowest latency, no bulk-copy engine work).
+// that half, computes P for it, and writes it into both CTAs' P buffers.  The
+// bulk transfers between the pair (partial scores, P halves) are bulk copies,
+// which the copy engine carries while the warps go on; the per-row reference
+// maxima and row sums go by st.async.  Both complete transaction bytes on the
+// receiver's mbarrier.
 //
 // Warp roles (224 threads; 352 for an FP8 cache):
 //   warp 0     TMA producer: Q once, then per page a block-table lookup and the
@@ -62,6 +64,7 @@ constexpr int kStages = 4;
 constexpr int kSinQuadBytes = 32 * 32 * 4;    // peer's partial S: 32 rows x 32 tokens of one quadrant
 constexpr int kSinBytes = 4 * kSinQuadBytes;
 constexpr int kPBytes = kRows * 128;    // P[128 rows x 64 tokens] bf16
+constexpr int kPHalfBytes = kPBytes / 2;  // one token half of P
 constexpr int kStageOff = 0;
 constexpr int kQStageOff = kStageOff + 2 * kStageBytes;  // Q's c_kv chunks land in stages 2-3, then go to TMEM
 static_assert(4 * kQChunkBytes <= 2 * kStageBytes, "Q staging");
@@ -359,16 +362,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         if (!wait_bar(ctl, &ctl->pv_ready[j & 1], (j >> 1) & 1, p, 5) ||
             !wait_bar(ctl, &ctl->checked[j & 1], (j >> 1) & 1, p, 7))
           break;
-        // The peer's P halves arrive by st.async, generic-proxy writes: the fence
-        // after the acquiring waits makes them visible to the MMA's operand reads.
-        fence_proxy_async_smem();
         tc_fence_after();
         const uint64_t v_desc = sdesc_sw128(kv_addr + (j & 3) * kStageBytes, kKvChunkBytes, 1024);
-        const uint64_t p_desc = sdesc_sw128(p_addr, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ss(tmem + kColO, p_desc + (uint64_t)((kk * 32) >> 4), v_desc + (uint64_t)((kk * 2048) >> 4),
-                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)  // A = P tokens 16kk..16kk+15: two 8-token chunks of one half
+          mma_bf16_ss(tmem + kColO, sdesc_noswz(p_addr + (kk >> 1) * kPHalfBytes + ((2 * kk) & 3) * 128, 128, 512),
+                      v_desc + (uint64_t)((kk * 2048) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&ctl->empty[j & 3]);      // stage free; O current through page j
         mma_commit_multicast(&ctl->p_free, 3);  // P reusable, in both CTAs
       }
@@ -462,8 +461,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     bool poisoned = !len_ok;
     bool ok = true;
 
-    // 16-byte chunk u (0..7, before the swizzle) of this thread's row of P buffer e.
-    auto p_chunk = [&](int u) -> uint8_t* { return sP + r * 128 + ((u ^ (r & 7)) << 4); };
+    // 16-byte chunk u (tokens 8u..8u+7) of this thread's row of P.  P is K-major
+    // without swizzle, laid out [token half][8-row group][8-token chunk][row][16 B],
+    // so a warp's 32 rows of one token half are 2 KB of contiguous bytes.
+    auto p_chunk = [&](int u) -> uint8_t* {
+      return sP + (u >> 2) * kPHalfBytes + (r >> 3) * 512 + (u & 3) * 128 + (r & 7) * 16;
+    };
+    uint8_t* p_mine = sP + (int)cta * kPHalfBytes + quad * 2048;  // this warp's rows of this CTA's half
 
     // S(jj) from TMEM: this CTA's token half stays in `own`; the peer's half is
     // staged in S_out and goes to the peer's S_in for this quadrant as one 4 KB
@@ -735,17 +739,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         ok = false;
         break;
       }
-      // Local rows first, fenced and signalled before the remote copies are
-      // issued, so that the fence does not wait on stores queued for the link.
+      // The warp's P rows go to the peer as one 2 KB bulk copy (the copy engine
+      // carries them; the warp does not stall on the pair's link), its rows'
+      // references by st.async.
 #pragma unroll
       for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(p_chunk(4 * (int)cta + u)) = pk[u];
-      fence_proxy_async_smem();  // local P rows (and any zeroed V rows) visible to the MMA
+      fence_proxy_async_smem();  // P rows (and any zeroed V rows) visible to the MMA and the copy engine
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&ctl->pv_ready[e], kPvReadyTx);
       const uint32_t pv_bar_peer = mapa_shared(smem_u32(&ctl->pv_ready[e]), peer);
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        st_async_v4(p_peer + (uint32_t)(p_chunk(4 * (int)cta + u) - sP), pk[u], pv_bar_peer);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&ctl->pv_ready[e], kPvReadyTx);
+        bulk_copy_to_peer(p_peer + (uint32_t)(p_mine - sP), p_mine, 2048, pv_bar_peer);
+      }
       st_async_u32(mapa_shared(smem_u32(&ctl->u_peer[e][r]), peer), __float_as_uint(u_cur), pv_bar_peer);
       u_prev = u_cur;
     }

@@ -298,6 +298,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Shared-memory matrix descriptor, no swizzle (8-row x 16-byte core matrices):
+// for a K-major operand, lbo = byte distance between core matrices adjacent in
+// K, sbo = between core matrices adjacent in M/N.
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
+         ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4,
 //   32-45 stride byte offset >> 4, 46-48 fixed 0b001, 61-63 layout (2 = 128B swizzle).
