@@ -197,7 +197,8 @@ __device__ __forceinline__ bool wait_bar(Ctl* c, uint64_t* bar, uint32_t parity,
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(), 1)
     split_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
-                       const __grid_constant__ CUtensorMap tm_kv, const DecodeParams p) {
+                       const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kv3,
+                       const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
@@ -271,6 +272,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_pages > 0) {
       prefetch_tmap(&tm_kv);
+      if (!kFp8) prefetch_tmap(&tm_kv3);
       // No L2 prefetch of upcoming pages: it goes through the same copy engine
       // as the pair's partial-score transfers and measured slower.
       const int qrow = b * p.rows + row0;
@@ -301,9 +303,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
           for (int k = 0; k < nch; ++k)
             tma_load_2d(stage + kRawOff + k * kRawBox, &tm_kv, land, (g0 + k) * 64, page * kPage);
         } else {
+          // The CTA's four c_kv chunks in one 3-D box (columns x rows x chunks),
+          // which lands as [chunk][row][128 B]; CTA 1's k_pe chunk in a 2-D box.
           mbar_arrive_expect_tx(land, nch * kKvChunkBytes);
-          for (int k = 0; k < nch; ++k)
-            tma_load_2d(stage + k * kKvChunkBytes, &tm_kv, land, (g0 + k) * 64, page * kPage);
+          tma_load_3d(stage, &tm_kv3, land, 0, page * kPage, g0);
+          if (nch == 5) tma_load_2d(stage + 4 * kKvChunkBytes, &tm_kv, land, 8 * 64, page * kPage);
         }
         issued = j + 1;
       }
@@ -856,10 +860,25 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D tensor map over a bf16 cache: {64 columns, rows, 9 chunks of 64 columns},
+// box {64, 64 rows, 4 chunks}, 128-byte swizzle.  The chunk dimension steps back
+// through each row (stride 128 B), so one box lands as four 8 KB chunk tiles.
+bool encode_kv_chunks(CUtensorMap* m, const void* base, uint64_t rows) {
+  EncodeFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, rows, kRow / 64};
+  cuuint64_t strides[2] = {(cuuint64_t)kRow * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)kPage, 4};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
-  CUtensorMap tm_qn, tm_qp, tm_kv;
+  CUtensorMap tm_qn, tm_qp, tm_kv, tm_kv3;
   const uint64_t q_rows = (uint64_t)p.batch * p.rows;
   const uint64_t kv_rows = (uint64_t)p.num_pages * kPage;
   if (!encode_2d(&tm_qn, p.q_nope, kKvLora, q_rows, p.q_nope_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128,
@@ -872,17 +891,20 @@ cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
                            : encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
                                        CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
+  // bf16 cache viewed as [chunk 0..8][row][64 columns]: row stride 1152 B, chunk stride 128 B.
+  if (!p.kv_fp8 && !encode_kv_chunks(&tm_kv3, p.kv, kv_rows)) return cudaErrorInvalidValue;
+  if (p.kv_fp8) tm_kv3 = tm_kv;  // unused on the FP8 path
   const dim3 grid(2 * p.row_groups, p.splits, p.batch);
   if (p.kv_fp8) {
     auto kern = split_kv_tc_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, block_threads<true>(), kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, p);
+    kern<<<grid, block_threads<true>(), kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, p);
   } else {
     auto kern = split_kv_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, block_threads<false>(), kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, p);
+    kern<<<grid, block_threads<false>(), kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, p);
   }
   return cudaGetLastError();
 }
