@@ -96,7 +96,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far above any legitimate wait
-constexpr int kCheckPos = 1;  // where in a page's iteration the previous page is checked
+constexpr int kCheckPos = 1;
+constexpr int kPrefetchDist = 0;     // pages ahead pulled into L2 (0: none)
+constexpr bool kPrefetchAlt = false;  // CTAs take turns prefetching (else CTA 0 alone)  // where in a page's iteration the previous page is checked
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
@@ -271,10 +273,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_pages > 0) {
+      auto pf_mine = [&](int j) { return kPrefetchAlt ? (int)cta == (j & 1) : cta == 0; };
       prefetch_tmap(&tm_kv);
       if (!kFp8) prefetch_tmap(&tm_kv3);
-      // No L2 prefetch of upcoming pages: it goes through the same copy engine
-      // as the pair's partial-score transfers and measured slower.
+      // Optional L2 prefetch of whole upcoming pages, kPrefetchDist ahead
+      // (a page is one contiguous block of the cache).
+      const int64_t page_bytes = (int64_t)kPage * kRow * (kFp8 ? 1 : 2);
+      auto prefetch = [&](int j, int pg) {
+        if (kPrefetchDist > 0 && pf_mine(j) && pg >= 0 && pg < p.num_pages)
+          prefetch_l2(static_cast<const uint8_t*>(p.kv) + pg * page_bytes, (uint32_t)page_bytes);
+      };
+      for (int j = 0; j < kPrefetchDist && j < n_pages; ++j)
+        if (pf_mine(j)) prefetch(j, bt_row[j]);
       const int qrow = b * p.rows + row0;
       mbar_arrive_expect_tx(&ctl->q_full, nch * kQChunkBytes);
       for (int k = 0; k < nch; ++k) {
@@ -290,9 +300,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         const int s = j & 3;
         const int page = next_page;
         if (j + 1 < n_pages) next_page = bt_row[j + 1];  // lookups ahead of the waits
+        const int jp = j + kPrefetchDist;
+        const int pf = (kPrefetchDist > 0 && jp < n_pages && pf_mine(jp)) ? bt_row[jp] : -1;
         // Stages 2-3 hold Q until the softmax warps have moved it into TMEM.
         if (j == 2 && !wait_bar(ctl, &ctl->q_tmem, 0, p, 17)) break;
         if (!wait_bar(ctl, &ctl->empty[s], ((j >> 2) & 1) ^ 1, p, 1)) break;
+        if (pf >= 0) prefetch(jp, pf);
         uint64_t* land = kFp8 ? &ctl->raw_full[s] : &ctl->full[s];
         uint8_t* stage = sKV + s * kStageBytes;
         if (page < 0 || page >= p.num_pages) {
@@ -787,36 +800,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       }
     }
     const int rows_here = min(kRows, p.rows - row0);
-    // O_c rows are TMEM lanes: stage 32 rows x 32 columns through shared memory
-    // (S_out and P, idle once the last PV has completed) so global stores run
-    // along the 512 columns.
-    float* tile = reinterpret_cast<float*>(sSout) + (warp - kSoftmaxWarp0) * (32 * 33);
+    // O_c rows are TMEM lanes: each warp stages 32 rows x 32 columns at a time
+    // through shared memory (S_out and P, idle once the last PV has completed) so
+    // that the global stores run along the columns.  The next chunk's TMEM load is
+    // in flight while a chunk is written out.
+    constexpr int kTileStride = 36;  // floats per staged row: 16-byte stores free of bank conflicts
+    float* tile = reinterpret_cast<float*>(sSout) + (warp - kSoftmaxWarp0) * (32 * kTileStride);
+    uint32_t v[2][16];
+    if (have_o) {
+      tmem_ld16(tmem + lane_base + kColO, v[0]);
+      tmem_ld16(tmem + lane_base + kColO + 16, v[1]);
+    }
 #pragma unroll 1
     for (int c0 = 0; c0 < 256; c0 += 32) {
-      uint32_t v[2][16];
+      float4 f[8];
       if (have_o) {
-        tmem_ld16(tmem + lane_base + kColO + c0, v[0]);
-        tmem_ld16(tmem + lane_base + kColO + c0 + 16, v[1]);
         tmem_ld_wait();
+        const float sc = il > 0.f ? il : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          f[u] = make_float4(__uint_as_float(v[u >> 2][(u & 3) * 4]) * sc, __uint_as_float(v[u >> 2][(u & 3) * 4 + 1]) * sc,
+                             __uint_as_float(v[u >> 2][(u & 3) * 4 + 2]) * sc,
+                             __uint_as_float(v[u >> 2][(u & 3) * 4 + 3]) * sc);
+        if (c0 + 32 < 256) {
+          tmem_ld16(tmem + lane_base + kColO + c0 + 32, v[0]);
+          tmem_ld16(tmem + lane_base + kColO + c0 + 48, v[1]);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) f[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (bad) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) f[u] = make_float4(NAN, NAN, NAN, NAN);
       }
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        float o = (have_o && il > 0.f) ? __uint_as_float(v[k >> 4][k & 15]) * il : 0.f;
-        if (bad) o = NAN;
-        tile[lane * 33 + k] = o;
-      }
+      for (int u = 0; u < 8; ++u) *reinterpret_cast<float4*>(tile + lane * kTileStride + 4 * u) = f[u];
       __syncwarp();
+      // Lane l writes column c0+l of the warp's 32 rows: one coalesced 128-byte
+      // row segment per store, addresses stepping by a constant row stride.
       const int dim = (int)cta * 256 + c0 + lane;
-#pragma unroll 4
-      for (int rr = 0; rr < 32; ++rr) {
-        const int row = quad * 32 + rr;
-        if (row >= rows_here) break;
-        const float o = tile[rr * 33 + lane];
-        const int64_t grow = grow0 + row;
-        if (p.splits == 1)
-          store_out(p, grow, dim, o);
-        else
-          p.partials[(grow * p.splits + split) * kPartRow + dim] = o;
+      const int nr = min(32, rows_here - quad * 32);  // rows of this warp that exist
+      const float* trow = tile + lane;
+      if (p.splits > 1) {
+        float* dst = p.partials + ((grow0 + quad * 32) * p.splits + split) * kPartRow + dim;
+        const int64_t step = (int64_t)p.splits * kPartRow;
+        if (nr == 32) {
+#pragma unroll
+          for (int rr = 0; rr < 32; ++rr) dst[rr * step] = trow[rr * kTileStride];
+        } else {
+          for (int rr = 0; rr < nr; ++rr) dst[rr * step] = trow[rr * kTileStride];
+        }
+      } else if (p.out_fp32) {
+        float* dst = reinterpret_cast<float*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
+        for (int rr = 0; rr < nr; ++rr) dst[rr * kKvLora] = trow[rr * kTileStride];
+      } else {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
+#pragma unroll 8
+        for (int rr = 0; rr < nr; ++rr) dst[rr * kKvLora] = __float2bfloat16_rn(trow[rr * kTileStride]);
       }
       __syncwarp();
     }
