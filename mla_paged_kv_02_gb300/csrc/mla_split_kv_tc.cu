@@ -838,28 +838,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       for (int u = 0; u < 8; ++u) *reinterpret_cast<float4*>(tile + lane * kTileStride + 4 * u) = f[u];
       __syncwarp();
       // Lane l writes column c0+l of the warp's 32 rows: one coalesced 128-byte
-      // row segment per store, addresses stepping by a constant row stride.
+      // row segment per store, addresses stepping by a constant row stride.  All
+      // 32 staged values are read first: with the loads interleaved, each would
+      // wait out the previous store (the compiler cannot tell the two apart).
+      float col[32];
+#pragma unroll
+      for (int rr = 0; rr < 32; ++rr) col[rr] = tile[rr * kTileStride + lane];
+      __syncwarp();  // the tile may be rewritten once every lane holds its column
       const int dim = (int)cta * 256 + c0 + lane;
       const int nr = min(32, rows_here - quad * 32);  // rows of this warp that exist
-      const float* trow = tile + lane;
       if (p.splits > 1) {
         float* dst = p.partials + ((grow0 + quad * 32) * p.splits + split) * kPartRow + dim;
         const int64_t step = (int64_t)p.splits * kPartRow;
-        if (nr == 32) {
 #pragma unroll
-          for (int rr = 0; rr < 32; ++rr) dst[rr * step] = trow[rr * kTileStride];
-        } else {
-          for (int rr = 0; rr < nr; ++rr) dst[rr * step] = trow[rr * kTileStride];
-        }
+        for (int rr = 0; rr < 32; ++rr)
+          if (rr < nr) dst[rr * step] = col[rr];
       } else if (p.out_fp32) {
         float* dst = reinterpret_cast<float*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
-        for (int rr = 0; rr < nr; ++rr) dst[rr * kKvLora] = trow[rr * kTileStride];
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr)
+          if (rr < nr) dst[rr * kKvLora] = col[rr];
       } else {
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
-#pragma unroll 8
-        for (int rr = 0; rr < nr; ++rr) dst[rr * kKvLora] = __float2bfloat16_rn(trow[rr * kTileStride]);
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr)
+          if (rr < nr) dst[rr * kKvLora] = __float2bfloat16_rn(col[rr]);
       }
-      __syncwarp();
     }
     tc_fence_before();
   }
