@@ -103,9 +103,11 @@ constexpr bool kPrefetchAlt = false;  // CTAs take turns prefetching (else CTA 0
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
 
-// Bytes the peer's warp of a quadrant delivers into pv_ready per page: its 32
-// rows' P halves (64 B each) and the references they were computed with.
-constexpr uint32_t kPvReadyTx = 32 * (64 + 4);
+// Bytes the peer's warp of a quadrant delivers per page: its 32 rows' P halves
+// (64 B each) into pv_ready, and the references they are computed with (4 B
+// each) into u_ready.
+constexpr uint32_t kPvReadyTx = 32 * 64;
+constexpr uint32_t kUReadyTx = 32 * 4;
 
 struct Ctl {
   uint64_t q_full;
@@ -118,7 +120,8 @@ struct Ctl {
   uint64_t sin_full[4];        // per quadrant: the peer's partial S landed (count 1 + 4 KB of st.async bytes)
   uint64_t sin_free[4];        // per quadrant: the peer consumed what this CTA sent (count 1, remote)
   uint64_t p_free;             // PV of the previous page done in both CTAs: P rewritable (count 2)
-  uint64_t pv_ready[2];        // local P halves written (count 4) + the peer's halves and references landed
+  uint64_t pv_ready[2];        // local P halves written (count 4) + the peer's halves landed
+  uint64_t u_ready[2];         // the peer's references for the page landed (count 4 + 512 B)
   uint64_t checked[2];         // the 4 local warps ran the page's reference check (count 4)
   uint64_t fin;                // the peer's row sums delivered (count 4 + 512 B)
   uint64_t drain;
@@ -251,6 +254,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     for (int e = 0; e < 2; ++e) {
       mbar_init(&ctl->pv_ready[e], 4);
       mbar_init(&ctl->checked[e], 4);
+      mbar_init(&ctl->u_ready[e], 4);
     }
     mbar_init(&ctl->p_free, 2);
     mbar_init(&ctl->fin, 4);
@@ -518,16 +522,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       return true;
     };
 
-    // Page k's reference check, run once both CTAs' P(k) and references are in
-    // and before PV(k) may be issued (the MMA waits for `checked`).
+    // Page k's reference check, run once the peer's references for page k are in
+    // and before PV(k) may be issued (the MMA waits for `checked`).  Only when a
+    // P half must be scaled does it also wait for the peer's P halves.
     auto check = [&](int k, float u_own) -> bool {
       const int e = k & 1;
-      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->pv_ready[e], (k >> 1) & 1, p, 11))) return false;
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->u_ready[e], (k >> 1) & 1, p, 11))) return false;
       const float u_oth = ctl->u_peer[e][r];
       const float an = fmaxf(a_ref, fmaxf(u_own, u_oth));
       const bool resc = k > 0 && an > a_ref;  // PV(0) overwrites O
       const bool fix_own = u_own < an, fix_oth = u_oth < an;
       if (__any_sync(0xffffffffu, resc || fix_own || fix_oth)) {
+        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->pv_ready[e], (k >> 1) & 1, p, 19))) return false;
         if (__any_sync(0xffffffffu, resc)) {
           // O holds exactly pages < k once PV(k-1) has completed.
           if (!__all_sync(0xffffffffu,
@@ -716,6 +722,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         r_ref = u;
       }
       const float u_cur = r_ref;
+      // This page's references go to the peer now, ahead of P, so that the peer's
+      // check of the page need not wait for the P transfer.
+      st_async_u32(mapa_shared(smem_u32(&ctl->u_peer[e][r]), peer), __float_as_uint(u_cur),
+                   mapa_shared(smem_u32(&ctl->u_ready[e]), peer));
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->u_ready[e], kUReadyTx);
       uint4 pk[4];
       float part[4] = {0.f, 0.f, 0.f, 0.f};
       if (fast) {
@@ -757,8 +768,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         break;
       }
       // The warp's P rows go to the peer as one 2 KB bulk copy (the copy engine
-      // carries them; the warp does not stall on the pair's link), its rows'
-      // references by st.async.
+      // carries them; the warp does not stall on the pair's link).
 #pragma unroll
       for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(p_chunk(4 * (int)cta + u)) = pk[u];
       fence_proxy_async_smem();  // P rows (and any zeroed V rows) visible to the MMA and the copy engine
@@ -768,7 +778,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         mbar_arrive_expect_tx(&ctl->pv_ready[e], kPvReadyTx);
         bulk_copy_to_peer(p_peer + (uint32_t)(p_mine - sP), p_mine, 2048, pv_bar_peer);
       }
-      st_async_u32(mapa_shared(smem_u32(&ctl->u_peer[e][r]), peer), __float_as_uint(u_cur), pv_bar_peer);
       u_prev = u_cur;
     }
     if (ok && n_pages >= 1 && !check(n_pages - 1, u_prev)) ok = false;
