@@ -96,7 +96,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far above any legitimate wait
-constexpr int kCheckPos = 1;
 constexpr int kPrefetchDist = 0;     // pages ahead pulled into L2 (0: none)
 constexpr bool kPrefetchAlt = false;  // CTAs take turns prefetching (else CTA 0 alone)  // where in a page's iteration the previous page is checked
 
@@ -626,12 +625,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       if (j + 1 < n_pages) page_next = bt_row[j + 1];
       const bool page_ok = page >= 0 && page < p.num_pages;
       poisoned |= !page_ok;
-      // The previous page's references are checked before this page's reference
-      // is settled; PV(j-1), and with it the release of its stage, waits for it.
-      if (kCheckPos == 0 && j >= 1 && !check(j - 1, u_prev)) {
-        ok = false;
-        break;
-      }
       float sv[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) sv[k] = sv_next[k];
@@ -683,18 +676,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       __syncwarp();  // every lane's S_in values are in registers
       if (lane == 0) mbar_arrive_cluster_relaxed(sin_free_peer);
 
-      if (kCheckPos == 1 && j >= 1 && !check(j - 1, u_prev)) {
+      // The previous page's references are checked (PV(j-1), and with it the
+      // release of its stage, waits for this), then this page's reference is
+      // settled and goes to the peer first, ahead of the larger transfers, so
+      // that the peer's check of this page need not wait for them.
+      if (j >= 1 && !check(j - 1, u_prev)) {
         ok = false;
         break;
       }
+      if (mx > r_ref + kRescaleThreshold) {  // false while every column is masked
+        const float u = ceilf(mx);
+        l_sum *= ex2(r_ref - u);
+        r_ref = u;
+      }
+      const float u_cur = r_ref;
+      st_async_u32(mapa_shared(smem_u32(&ctl->u_peer[e][r]), peer), __float_as_uint(u_cur),
+                   mapa_shared(smem_u32(&ctl->u_ready[e]), peer));
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->u_ready[e], kUReadyTx);
 
       // Next page's scores to the peer while this page's P is computed.
       if (j + 1 < n_pages && !take_s(j + 1, sv_next)) {
-        ok = false;
-        break;
-      }
-
-      if (kCheckPos == 2 && j >= 1 && !check(j - 1, u_prev)) {
         ok = false;
         break;
       }
@@ -716,17 +717,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         }
       }
 
-      if (mx > r_ref + kRescaleThreshold) {  // false while every column is masked
-        const float u = ceilf(mx);
-        l_sum *= ex2(r_ref - u);
-        r_ref = u;
-      }
-      const float u_cur = r_ref;
-      // This page's references go to the peer now, ahead of P, so that the peer's
-      // check of the page need not wait for the P transfer.
-      st_async_u32(mapa_shared(smem_u32(&ctl->u_peer[e][r]), peer), __float_as_uint(u_cur),
-                   mapa_shared(smem_u32(&ctl->u_ready[e]), peer));
-      if (lane == 0) mbar_arrive_expect_tx(&ctl->u_ready[e], kUReadyTx);
       uint4 pk[4];
       float part[4] = {0.f, 0.f, 0.f, 0.f};
       if (fast) {
