@@ -512,13 +512,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       const bool qrow_ok = w.row0 + r < p.rows;
       const int64_t qrow = (int64_t)w.b * p.rows + w.row0 + r;
       const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + qrow * p.q_nope_stride + g0 * 64);
+      constexpr int kQRounds = kFp8 ? 2 : 1;  // FP8 has fewer registers per thread to spare
+      constexpr int kQChunksPerRound = 4 / kQRounds;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {  // two chunks (256 B of the row) at a time
-        uint4 qv[16];
+      for (int h = 0; h < kQRounds; ++h) {
+        uint4 qv[8 * kQChunksPerRound];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) qv[u] = qrow_ok ? __ldg(src + h * 16 + u) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < 8 * kQChunksPerRound; ++u)
+          qv[u] = qrow_ok ? __ldg(src + h * 8 * kQChunksPerRound + u) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < kQChunksPerRound; ++k) {
           uint32_t wq[2][16];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -528,8 +531,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
             wq[u >> 2][(u & 3) * 4 + 2] = v.z;
             wq[u >> 2][(u & 3) * 4 + 3] = v.w;
           }
-          tmem_st16(tmem + lane_base + kColQ + (2 * h + k) * 32, wq[0]);
-          tmem_st16(tmem + lane_base + kColQ + (2 * h + k) * 32 + 16, wq[1]);
+          tmem_st16(tmem + lane_base + kColQ + (kQChunksPerRound * h + k) * 32, wq[0]);
+          tmem_st16(tmem + lane_base + kColQ + (kQChunksPerRound * h + k) * 32 + 16, wq[1]);
         }
       }
       if (nch == 5) {
