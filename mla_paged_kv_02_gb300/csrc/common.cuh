@@ -40,7 +40,6 @@ struct DecodeParams {
   int32_t* err;     // workspace header
   int batch, num_heads, q_len, rows;  // rows = num_heads * q_len per request
   int max_seq_len, splits, chunk_tokens, rows_per_cta, row_groups;
-  int cluster_slots;  // CTA pairs resident at once (SMs / 2): the persistent grid size
 };
 
 // Records the first device-side error of a call sequence (sticky until read).

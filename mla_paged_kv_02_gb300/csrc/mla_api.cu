@@ -78,7 +78,6 @@ mla_status_t fill_params(const mla_decode_plan_t* pl, const void* q_nope, int64_
   p->splits = pl->num_kv_splits;
   p->chunk_tokens = pl->chunk_tokens;
   p->rows_per_cta = pl->rows_per_cta;
-  p->cluster_slots = pl->num_sms / 2;
   p->row_groups = pl->row_groups;
   return MLA_OK;
 }

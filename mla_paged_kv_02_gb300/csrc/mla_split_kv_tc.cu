@@ -66,6 +66,8 @@ constexpr int kSinBytes = 4 * kSinQuadBytes;
 constexpr int kPBytes = kRows * 128;    // P[128 rows x 64 tokens] bf16
 constexpr int kPHalfBytes = kPBytes / 2;  // one token half of P
 constexpr int kStageOff = 0;
+constexpr int kQStageOff = kStageOff + 2 * kStageBytes;  // Q's c_kv chunks land in stages 2-3, then go to TMEM
+static_assert(4 * kQChunkBytes <= 2 * kStageBytes, "Q staging");
 constexpr int kSinOff = kStageOff + kStages * kStageBytes;  // S_in: the peer's partial scores, per quadrant
 constexpr int kSoutOff = kSinOff + kSinBytes;                 // S_out: partial scores staged for the peer
 constexpr int kPOff = kSoutOff + kSinBytes;                   // one P buffer
@@ -94,6 +96,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far above any legitimate wait
+constexpr int kPrefetchDist = 0;     // pages ahead pulled into L2 (0: none)
+constexpr bool kPrefetchAlt = false;  // CTAs take turns prefetching (else CTA 0 alone)  // where in a page's iteration the previous page is checked
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
@@ -105,6 +109,7 @@ constexpr uint32_t kPvReadyTx = 32 * 64;
 constexpr uint32_t kUReadyTx = 32 * 4;
 
 struct Ctl {
+  uint64_t q_full;
   uint64_t raw_full[kStages];
   uint64_t full[kStages];
   uint64_t empty[kStages];     // this CTA's PV of the stage's page has completed
@@ -118,13 +123,12 @@ struct Ctl {
   uint64_t u_ready[2];         // the peer's references for the page landed (count 4 + 512 B)
   uint64_t checked[2];         // the 4 local warps ran the page's reference check (count 4)
   uint64_t fin;                // the peer's row sums delivered (count 4 + 512 B)
-  uint64_t l_free;             // the peer has read this CTA's row sums (count 4, remote)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int poisoned;
   float u_peer[2][kRows];      // [P buffer][row]: reference the peer computed its half with
-  float l_peer[kRows];         // the peer's exp sums at the end of an item
+  float l_peer[kRows];         // the peer's exp sums at the end
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
@@ -194,39 +198,15 @@ __device__ __forceinline__ bool wait_bar(Ctl* c, uint64_t* bar, uint32_t parity,
   }
 }
 
-// One unit of work: 128 query rows (row group rg) of request b over split `split`.
-struct Item {
-  int b, split, rg, L, lo, first_page, n_pages, row0;
-  bool len_ok;
-  const int32_t* bt_row;  // block-table entries of the item's first page onwards
-};
-
-// Items are numbered ((b * splits) + split) * row_groups + rg; cluster c of G
-// takes items c, c + G, c + 2G, ...
-__device__ __forceinline__ Item make_item(const DecodeParams& p, int it) {
-  Item w;
-  w.rg = it % p.row_groups;
-  const int t = it / p.row_groups;
-  w.split = t % p.splits;
-  w.b = t / p.splits;
-  w.L = p.seq_lens[w.b];
-  w.len_ok = seq_len_ok(p, w.L);
-  w.lo = w.split * p.chunk_tokens;
-  const int hi = w.len_ok ? min(w.lo + p.chunk_tokens, w.L) : w.lo;
-  w.first_page = w.lo / kPage;
-  w.n_pages = hi > w.lo ? (hi + kPage - 1) / kPage - w.first_page : 0;
-  w.row0 = w.rg * kRows;
-  w.bt_row = p.block_table + (int64_t)w.b * p.bt_stride + w.first_page;
-  return w;
-}
-
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(), 1)
-    split_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kv3,
+    split_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
+                       const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kv3,
                        const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
+  uint8_t* sQ = smem + kQStageOff;  // Q staging (then stages 2-3)
   uint8_t* sKV = smem + kStageOff;
   uint8_t* sSin = smem + kSinOff;
   uint8_t* sQpe = smem + kQpeOff;
@@ -240,12 +220,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   const uint32_t peer = cta ^ 1u;
   const int nch = cta == 0 ? 4 : 5;        // 64-column chunks held
   const int g0 = cta == 0 ? 0 : 4;         // first global chunk
-  const int n_items = p.batch * p.splits * p.row_groups;
-  const int first_item = blockIdx.x >> 1;
-  const int item_step = gridDim.x >> 1;
+  const int rg = blockIdx.x >> 1;          // row group
+  const int split = blockIdx.y;
+  const int b = blockIdx.z;
+
+  const int L = p.seq_lens[b];
+  const bool len_ok = seq_len_ok(p, L);
+  const int lo = split * p.chunk_tokens;
+  const int hi = len_ok ? min(lo + p.chunk_tokens, L) : lo;
+  const int first_page = lo / kPage;
+  const int n_pages = hi > lo ? (hi + kPage - 1) / kPage - first_page : 0;
+  const int row0 = rg * kRows;
   const float kv_scale = (kFp8 && p.kv_scale) ? *p.kv_scale : 1.0f;
+  const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride + first_page;
 
   if (threadIdx.x == 0) {
+    mbar_init(&ctl->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctl->raw_full[s], 1);
       mbar_init(&ctl->full[s], kFp8 ? 4 : 1);
@@ -267,10 +257,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     }
     mbar_init(&ctl->p_free, 2);
     mbar_init(&ctl->fin, 4);
-    mbar_init(&ctl->l_free, 4);
     mbar_init(&ctl->drain, 2);  // both MMA-issuing threads' last commits
     ctl->abort = 0;
+    ctl->poisoned = len_ok ? 0 : 1;
     fence_mbarrier_init();
+    if (!len_ok && split == 0 && rg == 0 && cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, -1, L);
   }
   if (warp == 0) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -282,93 +273,98 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  // Every role walks the same items and pages in the same order; barrier phases
-  // follow running page and item counts, so they carry across items.
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && n_pages > 0) {
+      auto pf_mine = [&](int j) { return kPrefetchAlt ? (int)cta == (j & 1) : cta == 0; };
       prefetch_tmap(&tm_kv);
       if (!kFp8) prefetch_tmap(&tm_kv3);
-      int gp = 0;  // pages issued so far
-      bool ok = true;
-      for (int it = first_item; ok && it < n_items; it += item_step) {
-        const Item w = make_item(p, it);
-        if (!w.len_ok && w.split == 0 && w.rg == 0 && cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, w.b, -1, w.L);
-        int next_page = w.n_pages > 0 ? w.bt_row[0] : 0;
-        for (int j = 0; j < w.n_pages; ++j) {
-          const int s = gp & 3;
-          const int page = next_page;
-          if (j + 1 < w.n_pages) next_page = w.bt_row[j + 1];  // lookups ahead of the waits
-          if (!wait_bar(ctl, &ctl->empty[s], ((gp >> 2) & 1) ^ 1, p, 1)) {
-            ok = false;
-            break;
-          }
-          uint64_t* land = kFp8 ? &ctl->raw_full[s] : &ctl->full[s];
-          uint8_t* stage = sKV + s * kStageBytes;
-          if (page < 0 || page >= p.num_pages) {
-            if (cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, w.b, w.first_page + j, page);
-            mbar_arrive(land);  // nothing to load; consumers mask the whole page
-          } else if (kFp8) {
-            mbar_arrive_expect_tx(land, nch * kRawBox);
-            for (int k = 0; k < nch; ++k)
-              tma_load_2d(stage + kRawOff + k * kRawBox, &tm_kv, land, (g0 + k) * 64, page * kPage);
-          } else {
-            // The CTA's four c_kv chunks in one 3-D box (columns x rows x chunks),
-            // which lands as [chunk][row][128 B]; CTA 1's k_pe chunk in a 2-D box.
-            mbar_arrive_expect_tx(land, nch * kKvChunkBytes);
-            tma_load_3d(stage, &tm_kv3, land, 0, page * kPage, g0);
-            if (nch == 5) tma_load_2d(stage + 4 * kKvChunkBytes, &tm_kv, land, 8 * 64, page * kPage);
-          }
-          ++gp;
+      // Optional L2 prefetch of whole upcoming pages, kPrefetchDist ahead
+      // (a page is one contiguous block of the cache).
+      const int64_t page_bytes = (int64_t)kPage * kRow * (kFp8 ? 1 : 2);
+      auto prefetch = [&](int j, int pg) {
+        if (kPrefetchDist > 0 && pf_mine(j) && pg >= 0 && pg < p.num_pages)
+          prefetch_l2(static_cast<const uint8_t*>(p.kv) + pg * page_bytes, (uint32_t)page_bytes);
+      };
+      for (int j = 0; j < kPrefetchDist && j < n_pages; ++j)
+        if (pf_mine(j)) prefetch(j, bt_row[j]);
+      const int qrow = b * p.rows + row0;
+      mbar_arrive_expect_tx(&ctl->q_full, nch * kQChunkBytes);
+      for (int k = 0; k < nch; ++k) {
+        const int g = g0 + k;
+        if (g < 8)
+          tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, g * 64, qrow);
+        else
+          tma_load_2d(sQpe, &tm_qp, &ctl->q_full, 0, qrow);
+      }
+      int issued = 0;
+      int next_page = bt_row[0];
+      for (int j = 0; j < n_pages; ++j) {
+        const int s = j & 3;
+        const int page = next_page;
+        if (j + 1 < n_pages) next_page = bt_row[j + 1];  // lookups ahead of the waits
+        const int jp = j + kPrefetchDist;
+        const int pf = (kPrefetchDist > 0 && jp < n_pages && pf_mine(jp)) ? bt_row[jp] : -1;
+        // Stages 2-3 hold Q until the softmax warps have moved it into TMEM.
+        if (j == 2 && !wait_bar(ctl, &ctl->q_tmem, 0, p, 17)) break;
+        if (!wait_bar(ctl, &ctl->empty[s], ((j >> 2) & 1) ^ 1, p, 1)) break;
+        if (pf >= 0) prefetch(jp, pf);
+        uint64_t* land = kFp8 ? &ctl->raw_full[s] : &ctl->full[s];
+        uint8_t* stage = sKV + s * kStageBytes;
+        if (page < 0 || page >= p.num_pages) {
+          if (cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, first_page + j, page);
+          mbar_arrive(land);  // nothing to load; consumers mask the whole page
+        } else if (kFp8) {
+          mbar_arrive_expect_tx(land, nch * kRawBox);
+          for (int k = 0; k < nch; ++k)
+            tma_load_2d(stage + kRawOff + k * kRawBox, &tm_kv, land, (g0 + k) * 64, page * kPage);
+        } else {
+          // The CTA's four c_kv chunks in one 3-D box (columns x rows x chunks),
+          // which lands as [chunk][row][128 B]; CTA 1's k_pe chunk in a 2-D box.
+          mbar_arrive_expect_tx(land, nch * kKvChunkBytes);
+          tma_load_3d(stage, &tm_kv3, land, 0, page * kPage, g0);
+          if (nch == 5) tma_load_2d(stage + 4 * kKvChunkBytes, &tm_kv, land, 8 * 64, page * kPage);
         }
+        issued = j + 1;
       }
       // Never leave with copies in flight.
-      for (int g = max(0, gp - kStages); g < gp; ++g) {
-        uint64_t* land = kFp8 ? &ctl->raw_full[g & 3] : &ctl->full[g & 3];
+      for (int j = max(0, issued - kStages); j < issued; ++j) {
+        uint64_t* land = kFp8 ? &ctl->raw_full[j & 3] : &ctl->full[j & 3];
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(land), (g >> 2) & 1))
+        while (!mbar_try_wait(smem_u32(land), (j >> 2) & 1))
           if (globaltimer_ns() - t0 > kWaitLimitNs) break;
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK^T issuer
-    // QK(j) as soon as page j has landed, its S buffer is free and the item's Q
-    // is in place.  PV has a thread of its own (below), so a PV that becomes
-    // ready never waits behind the issue of a QK; the stage ring, S, S_in and P
-    // barriers bound how far QK runs ahead.
-    if (lane == 0) {
+    // QK(j) as soon as page j has landed and its S buffer is free.  PV has a
+    // thread of its own (below), so a PV that becomes ready never waits behind
+    // the issue of a QK; the stage ring, S, S_in and P barriers bound how far QK
+    // runs ahead.
+    if (lane == 0 && n_pages > 0) {
       const uint32_t kv_addr = smem_u32(sKV);
       const uint64_t qpe_desc = sdesc_sw128(smem_u32(sQpe), 16, 1024);
-      int gq = 0, nq_items = 0;
-      bool ok = true;
-      for (int it = first_item; ok && it < n_items; it += item_step) {
-        const Item w = make_item(p, it);
-        if (w.n_pages == 0) continue;
-        if (!wait_bar(ctl, &ctl->q_tmem, nq_items & 1, p, 2)) break;
-        ++nq_items;
-        for (int j = 0; j < w.n_pages; ++j, ++gq) {
-          if (!wait_bar(ctl, &ctl->full[gq & 3], (gq >> 2) & 1, p, 3) ||
-              !wait_bar(ctl, &ctl->s_free[gq & 1], ((gq >> 1) & 1) ^ 1, p, 4)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t k_desc = sdesc_sw128(kv_addr + (gq & 3) * kStageBytes, 16, 1024);
-          const uint32_t d = tmem + kColS + (gq & 1) * 64;
-          for (int k = 0; k < 4; ++k) {
+      bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
+      for (int j = 0; ok && j < n_pages; ++j) {
+        if (!wait_bar(ctl, &ctl->full[j & 3], (j >> 2) & 1, p, 3) ||
+            !wait_bar(ctl, &ctl->s_free[j & 1], ((j >> 1) & 1) ^ 1, p, 4))
+          break;
+        tc_fence_after();
+        const uint64_t k_desc = sdesc_sw128(kv_addr + (j & 3) * kStageBytes, 16, 1024);
+        const uint32_t d = tmem + kColS + (j & 1) * 64;
+        for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)  // A = Q chunk k from TMEM: 16 k per MMA = 8 columns
-              mma_bf16_ts(d, tmem + kColQ + k * 32 + kk * 8,
-                          k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4), kIdescQK, (k | kk) ? 1u : 0u);
-          }
-          if (nch == 5) {  // k_pe: A = q_pe from shared memory
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4),
-                          k_desc + (uint64_t)((4 * kKvChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
-          }
-          mma_commit(&ctl->s_full[gq & 1]);
+          for (int kk = 0; kk < 4; ++kk)  // A = Q chunk k from TMEM: 16 k per MMA = 8 columns
+            mma_bf16_ts(d, tmem + kColQ + k * 32 + kk * 8, k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4),
+                        kIdescQK, (k | kk) ? 1u : 0u);
         }
+        if (nch == 5) {  // k_pe: A = q_pe from shared memory
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4),
+                        k_desc + (uint64_t)((4 * kKvChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
+        }
+        mma_commit(&ctl->s_full[j & 1]);
       }
       mma_commit(&ctl->drain);  // every MMA of this thread has completed before TMEM is freed
       const uint64_t t0 = globaltimer_ns();
@@ -378,31 +374,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV issuer
     // PV(j) once both CTAs' P halves of page j are in and the local warps have
-    // checked its references (and scaled O or P where they moved).  An item's
-    // first PV overwrites O.
-    if (lane == 0) {
+    // checked its references (and scaled O or P where they moved).
+    if (lane == 0 && n_pages > 0) {
       const uint32_t kv_addr = smem_u32(sKV);
       const uint32_t p_addr = smem_u32(sP);
-      int gv = 0;
-      bool ok = true;
-      for (int it = first_item; ok && it < n_items; it += item_step) {
-        const Item w = make_item(p, it);
-        for (int j = 0; j < w.n_pages; ++j, ++gv) {
-          if (!wait_bar(ctl, &ctl->pv_ready[gv & 1], (gv >> 1) & 1, p, 5) ||
-              !wait_bar(ctl, &ctl->checked[gv & 1], (gv >> 1) & 1, p, 7)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t v_desc = sdesc_sw128(kv_addr + (gv & 3) * kStageBytes, kKvChunkBytes, 1024);
+      for (int j = 0; j < n_pages; ++j) {
+        if (!wait_bar(ctl, &ctl->pv_ready[j & 1], (j >> 1) & 1, p, 5) ||
+            !wait_bar(ctl, &ctl->checked[j & 1], (j >> 1) & 1, p, 7))
+          break;
+        tc_fence_after();
+        const uint64_t v_desc = sdesc_sw128(kv_addr + (j & 3) * kStageBytes, kKvChunkBytes, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // A = P tokens 16kk..16kk+15: two 8-token chunks of one half
-            mma_bf16_ss(tmem + kColO,
-                        sdesc_noswz(p_addr + (kk >> 1) * kPHalfBytes + ((2 * kk) & 3) * 128, 128, 512),
-                        v_desc + (uint64_t)((kk * 2048) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&ctl->empty[gv & 3]);       // stage free; O current through this page
-          mma_commit_multicast(&ctl->p_free, 3);  // P reusable, in both CTAs
-        }
+        for (int kk = 0; kk < 4; ++kk)  // A = P tokens 16kk..16kk+15: two 8-token chunks of one half
+          mma_bf16_ss(tmem + kColO, sdesc_noswz(p_addr + (kk >> 1) * kPHalfBytes + ((2 * kk) & 3) * 128, 128, 512),
+                      v_desc + (uint64_t)((kk * 2048) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&ctl->empty[j & 3]);      // stage free; O current through page j
+        mma_commit_multicast(&ctl->p_free, 3);  // P reusable, in both CTAs
       }
       mma_commit(&ctl->drain);
       const uint64_t t0 = globaltimer_ns();
@@ -413,52 +400,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // ------------------------------------------------------------ e4m3 -> bf16 converter
     const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
     const int units = nch * 64;                    // (chunk, token) pairs of 64 bytes
-    int gc = 0;
-    bool ok = true;
-    for (int it = first_item; ok && it < n_items; it += item_step) {
-      const Item w = make_item(p, it);
-      for (int j = 0; j < w.n_pages; ++j, ++gc) {
-        const int s = gc & 3;
-        if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[s], (gc >> 2) & 1, p, 9))) {
-          ok = false;
-          break;
+    for (int j = 0; j < n_pages; ++j) {
+      const int s = j & 3;
+      if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[s], (j >> 2) & 1, p, 9))) break;
+      uint8_t* stage = sKV + s * kStageBytes;
+      uint4 raw[3][4];
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const int u = ct + k * 128;
+        if (u < units) {
+          const uint4* src = reinterpret_cast<const uint4*>(stage + kRawOff + (u >> 6) * kRawBox + (u & 63) * 64);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) raw[k][q] = src[q];
         }
-        uint8_t* stage = sKV + s * kStageBytes;
-        uint4 raw[3][4];
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-          const int u = ct + k * 128;
-          if (u < units) {
-            const uint4* src = reinterpret_cast<const uint4*>(stage + kRawOff + (u >> 6) * kRawBox + (u & 63) * 64);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) raw[k][q] = src[q];
-          }
-        }
-        conv_sync();  // every raw byte is in registers before the bf16 writes overlap them
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-          const int u = ct + k * 128;
-          if (u < units) {
-            const int c = u >> 6, t = u & 63;
-            uint8_t* dst = stage + c * kKvChunkBytes + t * 128;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t wd[4] = {raw[k][q].x, raw[k][q].y, raw[k][q].z, raw[k][q].w};
-              uint32_t o[8];
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                o[2 * h] = e4m3x2_to_bf16x2((uint16_t)(wd[h] & 0xFFFFu));
-                o[2 * h + 1] = e4m3x2_to_bf16x2((uint16_t)(wd[h] >> 16));
-              }
-              *reinterpret_cast<uint4*>(dst + (((2 * q) ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        conv_sync();
-        if (lane == 0) mbar_arrive(&ctl->full[s]);
       }
+      conv_sync();  // every raw byte is in registers before the bf16 writes overlap them
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const int u = ct + k * 128;
+        if (u < units) {
+          const int c = u >> 6, t = u & 63;
+          uint8_t* dst = stage + c * kKvChunkBytes + t * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t w[4] = {raw[k][q].x, raw[k][q].y, raw[k][q].z, raw[k][q].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              o[2 * h] = e4m3x2_to_bf16x2((uint16_t)(w[h] & 0xFFFFu));
+              o[2 * h + 1] = e4m3x2_to_bf16x2((uint16_t)(w[h] >> 16));
+            }
+            *reinterpret_cast<uint4*>(dst + (((2 * q) ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      conv_sync();
+      if (lane == 0) mbar_arrive(&ctl->full[s]);
     }
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
     // ------------------------------------------------------------ softmax / exchange warpgroup
@@ -472,14 +451,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // halves, yet neither CTA sees the other's scores.  Each CTA computes with
     // its own reference r_ref (a whole number in the exp2 domain, so that any two
     // differ by a power of two), raised lazily to ceil(max) when a score exceeds
-    // it by more than 2^8.  Each page's references go to the peer; once both are
-    // in, each CTA takes the larger of the two and of the previous agreed value,
-    // scales O if the agreed value moved, and scales any P half computed against
-    // a lower reference (a raise, or a reference the CTA had not yet learnt from
-    // its peer) before PV.  Outside of raises, which occur on an item's first
-    // pages and when a row's max jumps, that check touches nothing.
+    // it by more than 2^8.  With every P half goes the reference it used; once
+    // both halves of page k are in, each CTA takes the larger of the two and of
+    // the previous agreed value, scales O if the agreed value moved, and scales
+    // any P half computed against a lower reference (a raise, or a reference the
+    // CTA had not yet learnt from its peer) before PV(k).  Outside of raises,
+    // which occur on a split's first pages and when a row's max jumps, that check
+    // touches nothing.
     const int quad = warp & 3;
     const int r = quad * 32 + lane;              // row within the group (TMEM lane)
+    const bool row_ok = row0 + r < p.rows;
+    const int qi = (row0 + r) / p.num_heads;
+    const int vis = L - p.q_len + 1 + qi;        // tokens this row may see
     const float sc2 = p.softmax_scale * kv_scale * kLog2e;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t col_own = kColS + 32 * cta;    // S columns of this CTA's token half (within a buffer)
@@ -491,8 +474,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     const uint32_t sin_full_peer = mapa_shared(smem_u32(&ctl->sin_full[quad]), peer);
     const uint32_t sin_free_peer = mapa_shared(smem_u32(&ctl->sin_free[quad]), peer);
     const uint32_t p_peer = mapa_shared(smem_u32(sP), peer);
-    int gs = 0;       // pages processed so far, over all items
-    int n_fin = 0;    // items finished (phase of `fin`)
+    float r_ref = -INFINITY;   // reference this CTA computes P with
+    float a_ref = -INFINITY;   // reference both CTAs agreed on, through the last checked page
+    float l_sum = 0.f;         // exp sum over this CTA's token halves, relative to r_ref
+    float u_prev = -INFINITY;  // reference the previous page was computed with
+    bool poisoned = !len_ok;
     bool ok = true;
 
     // 16-byte chunk u (tokens 8u..8u+7) of this thread's row of P.  P is K-major
@@ -503,439 +489,383 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     };
     uint8_t* p_mine = sP + (int)cta * kPHalfBytes + quad * 2048;  // this warp's rows of this CTA's half
 
-    // An item's Q rows, read straight from global memory (thread = row = TMEM
-    // lane): this CTA's four c_kv chunks into tensor memory as 2-bf16 columns, and
-    // in CTA 1 the q_pe chunk into shared memory in the 128B-swizzled layout the
-    // MMA reads.  Run once the previous item's last QK has completed (this warp
-    // has read its S), so its first QK can overlap the previous epilogue.
-    auto load_q = [&](const Item& w) {
-      const bool qrow_ok = w.row0 + r < p.rows;
-      const int64_t qrow = (int64_t)w.b * p.rows + w.row0 + r;
-      const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + qrow * p.q_nope_stride + g0 * 64);
-      constexpr int kQRounds = kFp8 ? 2 : 1;  // FP8 has fewer registers per thread to spare
-      constexpr int kQChunksPerRound = 4 / kQRounds;
+    // S(jj) from TMEM: this CTA's token half stays in `own`; the peer's half is
+    // staged in S_out and goes to the peer's S_in for this quadrant as one 4 KB
+    // bulk copy, once the peer has consumed the previous page's (which also means
+    // the previous copy has read S_out).  The copy engine carries the bytes, so
+    // the warp does not stall on the pair's link.
+    auto take_s = [&](int jj, float (&own)[32]) -> bool {
+      const int sb = jj & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[sb], (jj >> 1) & 1, p, 6))) return false;
+      tc_fence_after();
+      uint32_t mine[2][16], oth[2][16];
+      tmem_ld16(tmem + lane_base + col_own + sb * 64, mine[0]);
+      tmem_ld16(tmem + lane_base + col_own + sb * 64 + 16, mine[1]);
+      tmem_ld16(tmem + lane_base + col_oth + sb * 64, oth[0]);
+      tmem_ld16(tmem + lane_base + col_oth + sb * 64 + 16, oth[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
 #pragma unroll
-      for (int h = 0; h < kQRounds; ++h) {
-        uint4 qv[8 * kQChunksPerRound];
+      for (int k = 0; k < 32; ++k) own[k] = __uint_as_float(mine[k >> 4][k & 15]);
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_free[quad], (jj & 1) ^ 1, p, 13))) return false;
 #pragma unroll
-        for (int u = 0; u < 8 * kQChunksPerRound; ++u)
-          qv[u] = qrow_ok ? __ldg(src + h * 8 * kQChunksPerRound + u) : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(sout_row + ((u ^ (lane & 7)) << 4)) =
+            make_uint4(oth[u >> 2][(u & 3) * 4], oth[u >> 2][(u & 3) * 4 + 1], oth[u >> 2][(u & 3) * 4 + 2],
+                       oth[u >> 2][(u & 3) * 4 + 3]);
+      fence_proxy_async_smem();  // staged rows visible to the copy engine
+      __syncwarp();
+      if (lane == 0) bulk_copy_to_peer(sin_quad_peer, sout_quad, kSinQuadBytes, sin_full_peer);
+      return true;
+    };
+
+    // Page k's reference check, run once the peer's references for page k are in
+    // and before PV(k) may be issued (the MMA waits for `checked`).  Only when a
+    // P half must be scaled does it also wait for the peer's P halves.
+    auto check = [&](int k, float u_own) -> bool {
+      const int e = k & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->u_ready[e], (k >> 1) & 1, p, 11))) return false;
+      const float u_oth = ctl->u_peer[e][r];
+      const float an = fmaxf(a_ref, fmaxf(u_own, u_oth));
+      const bool resc = k > 0 && an > a_ref;  // PV(0) overwrites O
+      const bool fix_own = u_own < an, fix_oth = u_oth < an;
+      if (__any_sync(0xffffffffu, resc || fix_own || fix_oth)) {
+        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->pv_ready[e], (k >> 1) & 1, p, 19))) return false;
+        if (__any_sync(0xffffffffu, resc)) {
+          // O holds exactly pages < k once PV(k-1) has completed.
+          if (!__all_sync(0xffffffffu,
+                          wait_bar(ctl, &ctl->empty[(k - 1) & 3], ((k - 1) >> 2) & 1, p, 12)))
+            return false;
+          tc_fence_after();
+          const float f = resc ? ex2(a_ref - an) : 1.f;
+#pragma unroll 1
+          for (int g = 0; g < 16; ++g) {
+            uint32_t v[16];
+            const uint32_t ta = tmem + lane_base + kColO + g * 16;
+            tmem_ld16(ta, v);
+            tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < kQChunksPerRound; ++k) {
-          uint32_t wq[2][16];
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+            tmem_st16(ta, v);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+        }
+        // P halves computed against a lower reference; the factors are powers of two.
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const bool fix = h == (int)cta ? fix_own : fix_oth;
+          if (fix) {
+            const float f = ex2((h == (int)cta ? u_own : u_oth) - an);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4* c = reinterpret_cast<uint4*>(p_chunk(4 * h + u));
+              uint4 w = *c;
+              uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[i]));
+                __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
+                wv[i] = *reinterpret_cast<uint32_t*>(&y);
+              }
+              *c = w;
+            }
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      if (an > r_ref) {
+        l_sum *= ex2(r_ref - an);
+        r_ref = an;
+      }
+      a_ref = an;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->checked[e]);
+      return true;
+    };
+
+    // Q_c rows into tensor memory: thread = row = TMEM lane; the 128B-swizzled
+    // staging rows are un-swizzled into 2-bf16 columns, 32 columns per chunk.
+    if (n_pages > 0) {
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->q_full, 0, p, 18))) {
+        ok = false;
+      } else {
+        for (int k = 0; k < 4; ++k) {
+          const uint8_t* qrow = sQ + k * kQChunkBytes + r * 128;
+          uint32_t w[2][16];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const uint4 v = qv[k * 8 + u];
-            wq[u >> 2][(u & 3) * 4 + 0] = v.x;
-            wq[u >> 2][(u & 3) * 4 + 1] = v.y;
-            wq[u >> 2][(u & 3) * 4 + 2] = v.z;
-            wq[u >> 2][(u & 3) * 4 + 3] = v.w;
+            const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((u ^ (r & 7)) << 4));
+            w[u >> 2][(u & 3) * 4 + 0] = v.x;
+            w[u >> 2][(u & 3) * 4 + 1] = v.y;
+            w[u >> 2][(u & 3) * 4 + 2] = v.z;
+            w[u >> 2][(u & 3) * 4 + 3] = v.w;
           }
-          tmem_st16(tmem + lane_base + kColQ + (kQChunksPerRound * h + k) * 32, wq[0]);
-          tmem_st16(tmem + lane_base + kColQ + (kQChunksPerRound * h + k) * 32 + 16, wq[1]);
+          tmem_st16(tmem + lane_base + kColQ + k * 32, w[0]);
+          tmem_st16(tmem + lane_base + kColQ + k * 32 + 16, w[1]);
         }
+        tmem_st_wait();
       }
-      if (nch == 5) {
-        const uint4* src_pe = reinterpret_cast<const uint4*>(p.q_pe + qrow * p.q_pe_stride);
-        uint4 pe[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) pe[u] = qrow_ok ? __ldg(src_pe + u) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(sQpe + r * 128 + ((u ^ (r & 7)) << 4)) = pe[u];
-        fence_proxy_async_smem();  // q_pe rows visible to the MMA
-      }
-      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->q_tmem);
-    };
-
-    if (first_item < n_items) {
-      const Item w0 = make_item(p, first_item);
-      if (w0.n_pages > 0) load_q(w0);
     }
 
-    for (int it = first_item; it < n_items; it += item_step) {
-      const Item w = make_item(p, it);
-      const int n_pages = w.n_pages;
-      const int L = w.L;
-      const bool row_ok = w.row0 + r < p.rows;
-      const int qi = (w.row0 + r) / p.num_heads;
-      const int vis = L - p.q_len + 1 + qi;  // tokens this row may see
-      float r_ref = -INFINITY;   // reference this CTA computes P with
-      float a_ref = -INFINITY;   // reference both CTAs agreed on, through the last checked page
-      float l_sum = 0.f;         // exp sum over this CTA's token halves, relative to r_ref
-      float u_prev = -INFINITY;  // reference the previous page was computed with
-      bool poisoned = !w.len_ok;
-      const int g_first = gs;    // running index of the item's first page
-
-      // S(g) from TMEM: this CTA's token half stays in `own`; the peer's half is
-      // staged in S_out and goes to the peer's S_in for this quadrant as one 4 KB
-      // bulk copy, once the peer has consumed the previous page's (which also
-      // means the previous copy has read S_out).  The copy engine carries the
-      // bytes, so the warp does not stall on the pair's link.
-      auto take_s = [&](int g, float (&own)[32]) -> bool {
-        const int sb = g & 1;
-        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[sb], (g >> 1) & 1, p, 6))) return false;
-        tc_fence_after();
-        uint32_t mine[2][16], oth[2][16];
-        tmem_ld16(tmem + lane_base + col_own + sb * 64, mine[0]);
-        tmem_ld16(tmem + lane_base + col_own + sb * 64 + 16, mine[1]);
-        tmem_ld16(tmem + lane_base + col_oth + sb * 64, oth[0]);
-        tmem_ld16(tmem + lane_base + col_oth + sb * 64 + 16, oth[1]);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
+    // Block-table entries are loaded one page ahead: a global load consumed in
+    // the same iteration would stall every page for a full memory latency.
+    int page_next = n_pages > 0 ? bt_row[0] : 0;
+    float sv_next[32];
+    if (ok && n_pages > 0 && !take_s(0, sv_next)) ok = false;
+    for (int j = 0; ok && j < n_pages; ++j) {
+      const int e = j & 1;   // pv_ready / checked / peer references of this page
+      const int tok0 = lo + j * kPage;  // lo is page aligned
+      const int page = page_next;
+      if (j + 1 < n_pages) page_next = bt_row[j + 1];
+      const bool page_ok = page >= 0 && page < p.num_pages;
+      poisoned |= !page_ok;
+      float sv[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) own[k] = __uint_as_float(mine[k >> 4][k & 15]);
-        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_free[quad], (g & 1) ^ 1, p, 13))) return false;
+      for (int k = 0; k < 32; ++k) sv[k] = sv_next[k];
+
+      // The peer's partial of this CTA's token half.  Pages that every row of the
+      // warp sees in full (all but a split's last page, normally) take a fast
+      // path: add and max on raw scores (the scale is positive, so max commutes
+      // with it), then p = 2^(s*scale - ref) in one FMA + ex2.  Other pages mask
+      // and scale first; masked columns, possibly NaN garbage, become -inf and
+      // then exactly 0.
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->sin_full[quad], kSinQuadBytes);
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_full[quad], j & 1, p, 14))) {
+        ok = false;
+        break;
+      }
+      const int tok_c = tok0 + 32 * (int)cta;
+      const int n_vis = (page_ok && row_ok) ? min(max(vis - tok_c, 0), 32) : 0;
+      const bool fast = __all_sync(0xffffffffu, n_vis == 32);
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      {
+        const float4* src = reinterpret_cast<const float4*>(sin_row);
+        if (fast) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 v = src[u ^ (lane & 7)];
+            sv[4 * u] += v.x;
+            sv[4 * u + 1] += v.y;
+            sv[4 * u + 2] += v.z;
+            sv[4 * u + 3] += v.w;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mq[k] = fmaxf(mq[k], sv[4 * u + k]);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 v = src[u ^ (lane & 7)];
+            const float a[4] = {sv[4 * u] + v.x, sv[4 * u + 1] + v.y, sv[4 * u + 2] + v.z, sv[4 * u + 3] + v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float x = (4 * u + k < n_vis) ? a[k] * sc2 : -INFINITY;
+              sv[4 * u + k] = x;
+              mq[k] = fmaxf(mq[k], x);
+            }
+          }
+        }
+      }
+      float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      if (fast) mx *= sc2;
+      __syncwarp();  // every lane's S_in values are in registers
+      if (lane == 0) mbar_arrive_cluster_relaxed(sin_free_peer);
+
+      // The previous page's references are checked (PV(j-1), and with it the
+      // release of its stage, waits for this), then this page's reference is
+      // settled and goes to the peer first, ahead of the larger transfers, so
+      // that the peer's check of this page need not wait for them.
+      if (j >= 1 && !check(j - 1, u_prev)) {
+        ok = false;
+        break;
+      }
+      if (mx > r_ref + kRescaleThreshold) {  // false while every column is masked
+        const float u = ceilf(mx);
+        l_sum *= ex2(r_ref - u);
+        r_ref = u;
+      }
+      const float u_cur = r_ref;
+      st_async_u32(mapa_shared(smem_u32(&ctl->u_peer[e][r]), peer), __float_as_uint(u_cur),
+                   mapa_shared(smem_u32(&ctl->u_ready[e]), peer));
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->u_ready[e], kUReadyTx);
+
+      // Next page's scores to the peer while this page's P is computed.
+      if (j + 1 < n_pages && !take_s(j + 1, sv_next)) {
+        ok = false;
+        break;
+      }
+
+      // V rows of tokens at or past L (or of a page that was never loaded) may
+      // hold anything, NaN included; zero this CTA's 256 V columns of them.
+      // Thread t of the group clears half of token row t/2.
+      const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
+      if (n_valid < kPage) {
+        const int t = r >> 1;
+        if (t >= n_valid) {
+          uint8_t* stage = sKV + (j & 3) * kStageBytes;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint4* rowp = reinterpret_cast<uint4*>(stage + ((r & 1) * 2 + c) * kKvChunkBytes + t * 128);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) rowp[u] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+
+      uint4 pk[4];
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      if (fast) {
+        const float nm = -r_ref;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t w[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float p0 = ex2(fmaf(sv[u * 8 + 2 * h], sc2, nm));
+            const float p1 = ex2(fmaf(sv[u * 8 + 2 * h + 1], sc2, nm));
+            part[h] += p0 + p1;
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            w[h] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t w[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
+            const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - r_ref);
+            const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - r_ref);
+            part[h] += p0 + p1;
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            w[h] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      l_sum += (part[0] + part[1]) + (part[2] + part[3]);
+
+      // Both CTAs' PV of page j-1 must be done before P is rewritten.
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->p_free, (j & 1) ^ 1, p, 15))) {
+        ok = false;
+        break;
+      }
+      // The warp's P rows go to the peer as one 2 KB bulk copy (the copy engine
+      // carries them; the warp does not stall on the pair's link).
+#pragma unroll
+      for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(p_chunk(4 * (int)cta + u)) = pk[u];
+      fence_proxy_async_smem();  // P rows (and any zeroed V rows) visible to the MMA and the copy engine
+      __syncwarp();
+      const uint32_t pv_bar_peer = mapa_shared(smem_u32(&ctl->pv_ready[e]), peer);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&ctl->pv_ready[e], kPvReadyTx);
+        bulk_copy_to_peer(p_peer + (uint32_t)(p_mine - sP), p_mine, 2048, pv_bar_peer);
+      }
+      u_prev = u_cur;
+    }
+    if (ok && n_pages >= 1 && !check(n_pages - 1, u_prev)) ok = false;
+    ok = !wg_sync_or(!ok);  // the epilogue decides as one group
+
+    // ------------------------------------------------------------ epilogue
+    // Row sums of both token halves: every row's partial goes to the peer.
+    st_async_u32(mapa_shared(smem_u32(&ctl->l_peer[r]), peer), __float_as_uint(l_sum),
+                 mapa_shared(smem_u32(&ctl->fin), peer));
+    if (lane == 0) mbar_arrive_expect_tx(&ctl->fin, 32 * 4);
+    if (poisoned) atomicOr(&ctl->poisoned, 1);
+    bool fail = !wait_bar(ctl, &ctl->fin, 0, p, 16);
+    fail |= !ok || (n_pages > 0 && !wait_bar(ctl, &ctl->empty[(n_pages - 1) & 3], ((n_pages - 1) >> 2) & 1, p, 8));
+    fail = wg_sync_or(fail);
+    tc_fence_after();
+    __syncwarp();
+    const bool have_o = !fail && n_pages > 0;
+    const bool bad = ctl->poisoned != 0 || fail;
+    const float l_tot = l_sum + ctl->l_peer[r];
+    const bool has = l_tot > 0.f;
+    const float il = has ? kv_scale / l_tot : 0.f;
+    const int64_t grow0 = (int64_t)b * p.rows + row0;
+    if (cta == 0 && row_ok) {
+      const float lv = bad ? NAN : (has ? (r_ref + lg2(l_tot)) * kLn2 : -INFINITY);
+      if (p.splits == 1) {
+        if (p.lse) p.lse[grow0 + r] = lv;
+      } else {
+        p.partials[((grow0 + r) * p.splits + split) * kPartRow + kKvLora] = lv;
+      }
+    }
+    const int rows_here = min(kRows, p.rows - row0);
+    // O_c rows are TMEM lanes: each warp stages 32 rows x 32 columns at a time
+    // through shared memory (S_out and P, idle once the last PV has completed) so
+    // that the global stores run along the columns.  The next chunk's TMEM load is
+    // in flight while a chunk is written out.
+    constexpr int kTileStride = 36;  // floats per staged row: 16-byte stores free of bank conflicts
+    float* tile = reinterpret_cast<float*>(sSout) + (warp - kSoftmaxWarp0) * (32 * kTileStride);
+    uint32_t v[2][16];
+    if (have_o) {
+      tmem_ld16(tmem + lane_base + kColO, v[0]);
+      tmem_ld16(tmem + lane_base + kColO + 16, v[1]);
+    }
+#pragma unroll 1
+    for (int c0 = 0; c0 < 256; c0 += 32) {
+      float4 f[8];
+      if (have_o) {
+        tmem_ld_wait();
+        const float sc = il > 0.f ? il : 0.f;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(sout_row + ((u ^ (lane & 7)) << 4)) =
-              make_uint4(oth[u >> 2][(u & 3) * 4], oth[u >> 2][(u & 3) * 4 + 1], oth[u >> 2][(u & 3) * 4 + 2],
-                         oth[u >> 2][(u & 3) * 4 + 3]);
-        fence_proxy_async_smem();  // staged rows visible to the copy engine
-        __syncwarp();
-        if (lane == 0) bulk_copy_to_peer(sin_quad_peer, sout_quad, kSinQuadBytes, sin_full_peer);
-        return true;
-      };
-
-      // Reference check of the item's page k (running index g), run once the
-      // peer's references for it are in and before its PV may be issued (the MMA
-      // waits for `checked`).  Only when a P half must be scaled does it also
-      // wait for the peer's P halves.
-      auto check = [&](int k, int g, float u_own) -> bool {
-        const int e = g & 1;
-        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->u_ready[e], (g >> 1) & 1, p, 11))) return false;
-        const float u_oth = ctl->u_peer[e][r];
-        const float an = fmaxf(a_ref, fmaxf(u_own, u_oth));
-        const bool resc = k > 0 && an > a_ref;  // the item's first PV overwrites O
-        const bool fix_own = u_own < an, fix_oth = u_oth < an;
-        if (__any_sync(0xffffffffu, resc || fix_own || fix_oth)) {
-          if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->pv_ready[e], (g >> 1) & 1, p, 19))) return false;
-          if (__any_sync(0xffffffffu, resc)) {
-            // O holds exactly the item's pages < k once the previous PV has completed.
-            if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->empty[(g - 1) & 3], ((g - 1) >> 2) & 1, p, 12)))
-              return false;
-            tc_fence_after();
-            const float f = resc ? ex2(a_ref - an) : 1.f;
-#pragma unroll 1
-            for (int q = 0; q < 16; ++q) {
-              uint32_t v[16];
-              const uint32_t ta = tmem + lane_base + kColO + q * 16;
-              tmem_ld16(ta, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-              tmem_st16(ta, v);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-          }
-          // P halves computed against a lower reference; the factors are powers of two.
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const bool fix = h == (int)cta ? fix_own : fix_oth;
-            if (fix) {
-              const float f = ex2((h == (int)cta ? u_own : u_oth) - an);
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                uint4* c = reinterpret_cast<uint4*>(p_chunk(4 * h + u));
-                uint4 wv4 = *c;
-                uint32_t* wv = reinterpret_cast<uint32_t*>(&wv4);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[i]));
-                  __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
-                  wv[i] = *reinterpret_cast<uint32_t*>(&y);
-                }
-                *c = wv4;
-              }
-            }
-          }
-          fence_proxy_async_smem();
+          f[u] = make_float4(__uint_as_float(v[u >> 2][(u & 3) * 4]) * sc, __uint_as_float(v[u >> 2][(u & 3) * 4 + 1]) * sc,
+                             __uint_as_float(v[u >> 2][(u & 3) * 4 + 2]) * sc,
+                             __uint_as_float(v[u >> 2][(u & 3) * 4 + 3]) * sc);
+        if (c0 + 32 < 256) {
+          tmem_ld16(tmem + lane_base + kColO + c0 + 32, v[0]);
+          tmem_ld16(tmem + lane_base + kColO + c0 + 48, v[1]);
         }
-        if (an > r_ref) {
-          l_sum *= ex2(r_ref - an);
-          r_ref = an;
-        }
-        a_ref = an;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->checked[e]);
-        return true;
-      };
-
-      // Block-table entries are loaded one page ahead: a global load consumed in
-      // the same iteration would stall every page for a full memory latency.
-      int page_next = n_pages > 0 ? w.bt_row[0] : 0;
-      float sv_next[32];
-      if (ok && n_pages > 0 && !take_s(g_first, sv_next)) ok = false;
-      for (int j = 0; ok && j < n_pages; ++j) {
-        const int g = g_first + j;
-        const int e = g & 1;              // pv_ready / checked / peer references of this page
-        const int tok0 = w.lo + j * kPage;  // lo is page aligned
-        const int page = page_next;
-        if (j + 1 < n_pages) page_next = w.bt_row[j + 1];
-        const bool page_ok = page >= 0 && page < p.num_pages;
-        poisoned |= !page_ok;
-        float sv[32];
+      } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) sv[k] = sv_next[k];
-
-        // The peer's partial of this CTA's token half.  Pages that every row of the
-        // warp sees in full (all but an item's last page, normally) take a fast
-        // path: add and max on raw scores (the scale is positive, so max commutes
-        // with it), then p = 2^(s*scale - ref) in one FMA + ex2.  Other pages mask
-        // and scale first; masked columns, possibly NaN garbage, become -inf and
-        // then exactly 0.
-        if (lane == 0) mbar_arrive_expect_tx(&ctl->sin_full[quad], kSinQuadBytes);
-        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_full[quad], g & 1, p, 14))) {
-          ok = false;
-          break;
-        }
-        const int tok_c = tok0 + 32 * (int)cta;
-        const int n_vis = (page_ok && row_ok) ? min(max(vis - tok_c, 0), 32) : 0;
-        const bool fast = __all_sync(0xffffffffu, n_vis == 32);
-        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        {
-          const float4* src = reinterpret_cast<const float4*>(sin_row);
-          if (fast) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float4 v = src[u ^ (lane & 7)];
-              sv[4 * u] += v.x;
-              sv[4 * u + 1] += v.y;
-              sv[4 * u + 2] += v.z;
-              sv[4 * u + 3] += v.w;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) mq[k] = fmaxf(mq[k], sv[4 * u + k]);
-            }
-          } else {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float4 v = src[u ^ (lane & 7)];
-              const float a[4] = {sv[4 * u] + v.x, sv[4 * u + 1] + v.y, sv[4 * u + 2] + v.z, sv[4 * u + 3] + v.w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float x = (4 * u + k < n_vis) ? a[k] * sc2 : -INFINITY;
-                sv[4 * u + k] = x;
-                mq[k] = fmaxf(mq[k], x);
-              }
-            }
-          }
-        }
-        float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-        if (fast) mx *= sc2;
-        __syncwarp();  // every lane's S_in values are in registers
-        if (lane == 0) mbar_arrive_cluster_relaxed(sin_free_peer);
-
-        // The previous page's references are checked (its PV, and with it the
-        // release of its stage, waits for this), then this page's reference is
-        // settled and goes to the peer first, ahead of the larger transfers, so
-        // that the peer's check of this page need not wait for them.
-        if (j >= 1 && !check(j - 1, g - 1, u_prev)) {
-          ok = false;
-          break;
-        }
-        if (mx > r_ref + kRescaleThreshold) {  // false while every column is masked
-          const float u = ceilf(mx);
-          l_sum *= ex2(r_ref - u);
-          r_ref = u;
-        }
-        const float u_cur = r_ref;
-        st_async_u32(mapa_shared(smem_u32(&ctl->u_peer[e][r]), peer), __float_as_uint(u_cur),
-                     mapa_shared(smem_u32(&ctl->u_ready[e]), peer));
-        if (lane == 0) mbar_arrive_expect_tx(&ctl->u_ready[e], kUReadyTx);
-
-        // Next page's scores to the peer while this page's P is computed.
-        if (j + 1 < n_pages && !take_s(g + 1, sv_next)) {
-          ok = false;
-          break;
-        }
-
-        // V rows of tokens at or past L (or of a page that was never loaded) may
-        // hold anything, NaN included; zero this CTA's 256 V columns of them.
-        // Thread t of the group clears half of token row t/2.
-        const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
-        if (n_valid < kPage) {
-          const int t = r >> 1;
-          if (t >= n_valid) {
-            uint8_t* stage = sKV + (g & 3) * kStageBytes;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              uint4* rowp = reinterpret_cast<uint4*>(stage + ((r & 1) * 2 + c) * kKvChunkBytes + t * 128);
-#pragma unroll
-              for (int u = 0; u < 8; ++u) rowp[u] = make_uint4(0, 0, 0, 0);
-            }
-          }
-        }
-
-        uint4 pk[4];
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
-        if (fast) {
-          const float nm = -r_ref;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint32_t wd[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const float p0 = ex2(fmaf(sv[u * 8 + 2 * h], sc2, nm));
-              const float p1 = ex2(fmaf(sv[u * 8 + 2 * h + 1], sc2, nm));
-              part[h] += p0 + p1;
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-              wd[h] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            pk[u] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint32_t wd[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const float x0 = sv[u * 8 + 2 * h], x1 = sv[u * 8 + 2 * h + 1];
-              const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - r_ref);
-              const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - r_ref);
-              part[h] += p0 + p1;
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-              wd[h] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            pk[u] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-          }
-        }
-        l_sum += (part[0] + part[1]) + (part[2] + part[3]);
-
-        // Both CTAs' PV of the previous page must be done before P is rewritten.
-        if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->p_free, (g & 1) ^ 1, p, 15))) {
-          ok = false;
-          break;
-        }
-        // The warp's P rows go to the peer as one 2 KB bulk copy (the copy engine
-        // carries them; the warp does not stall on the pair's link).
-#pragma unroll
-        for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(p_chunk(4 * (int)cta + u)) = pk[u];
-        fence_proxy_async_smem();  // P rows (and any zeroed V rows) visible to the MMA and the copy engine
-        __syncwarp();
-        const uint32_t pv_bar_peer = mapa_shared(smem_u32(&ctl->pv_ready[e]), peer);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&ctl->pv_ready[e], kPvReadyTx);
-          bulk_copy_to_peer(p_peer + (uint32_t)(p_mine - sP), p_mine, 2048, pv_bar_peer);
-        }
-        u_prev = u_cur;
+        for (int u = 0; u < 8; ++u) f[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      if (ok && n_pages >= 1 && !check(n_pages - 1, g_first + n_pages - 1, u_prev)) ok = false;
-      gs = g_first + n_pages;
-      ok = !wg_sync_or(!ok);  // the epilogue decides as one group
-
-      // The next item's Q now, so that its first QK runs during this epilogue.
-      if (ok && it + item_step < n_items) {
-        const Item nx = make_item(p, it + item_step);
-        if (nx.n_pages > 0) load_q(nx);
+      if (bad) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) f[u] = make_float4(NAN, NAN, NAN, NAN);
       }
-
-      // -------------------------------------------------------- item epilogue
-      // Row sums of both token halves: every row's partial goes to the peer, once
-      // the peer has read the previous item's (an item without pages exchanges
-      // nothing else that would order the two).
-      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->l_free, (n_fin & 1) ^ 1, p, 20))) ok = false;
-      st_async_u32(mapa_shared(smem_u32(&ctl->l_peer[r]), peer), __float_as_uint(l_sum),
-                   mapa_shared(smem_u32(&ctl->fin), peer));
-      if (lane == 0) mbar_arrive_expect_tx(&ctl->fin, 32 * 4);
-      bool fail = !wait_bar(ctl, &ctl->fin, n_fin & 1, p, 16);
-      ++n_fin;
-      fail |= !ok || (n_pages > 0 && !wait_bar(ctl, &ctl->empty[(gs - 1) & 3], ((gs - 1) >> 2) & 1, p, 8));
-      fail = wg_sync_or(fail);
-      const bool bad = wg_sync_or(poisoned) || fail;
-      tc_fence_after();
+#pragma unroll
+      for (int u = 0; u < 8; ++u) *reinterpret_cast<float4*>(tile + lane * kTileStride + 4 * u) = f[u];
       __syncwarp();
-      const bool have_o = !fail && n_pages > 0;
-      const float l_tot = l_sum + ctl->l_peer[r];
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&ctl->l_free), peer));
-      const bool has = l_tot > 0.f;
-      const float il = has ? kv_scale / l_tot : 0.f;
-      const int64_t grow0 = (int64_t)w.b * p.rows + w.row0;
-      if (cta == 0 && row_ok) {
-        const float lv = bad ? NAN : (has ? (r_ref + lg2(l_tot)) * kLn2 : -INFINITY);
-        if (p.splits == 1) {
-          if (p.lse) p.lse[grow0 + r] = lv;
-        } else {
-          p.partials[((grow0 + r) * p.splits + w.split) * kPartRow + kKvLora] = lv;
-        }
+      // Lane l writes column c0+l of the warp's 32 rows: one coalesced 128-byte
+      // row segment per store, addresses stepping by a constant row stride.  All
+      // 32 staged values are read first: with the loads interleaved, each would
+      // wait out the previous store (the compiler cannot tell the two apart).
+      float col[32];
+#pragma unroll
+      for (int rr = 0; rr < 32; ++rr) col[rr] = tile[rr * kTileStride + lane];
+      __syncwarp();  // the tile may be rewritten once every lane holds its column
+      const int dim = (int)cta * 256 + c0 + lane;
+      const int nr = min(32, rows_here - quad * 32);  // rows of this warp that exist
+      if (p.splits > 1) {
+        float* dst = p.partials + ((grow0 + quad * 32) * p.splits + split) * kPartRow + dim;
+        const int64_t step = (int64_t)p.splits * kPartRow;
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr)
+          if (rr < nr) dst[rr * step] = col[rr];
+      } else if (p.out_fp32) {
+        float* dst = reinterpret_cast<float*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr)
+          if (rr < nr) dst[rr * kKvLora] = col[rr];
+      } else {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr)
+          if (rr < nr) dst[rr * kKvLora] = __float2bfloat16_rn(col[rr]);
       }
-      const int rows_here = min(kRows, p.rows - w.row0);
-      // O_c rows are TMEM lanes: each warp stages 32 rows x 32 columns at a time
-      // through its quadrant of S_out (idle between items) so that the global
-      // stores run along the columns.  The staging rows are 128 B with their
-      // 16-byte chunks XOR-swizzled by row, so neither the row-wise writes nor the
-      // column-wise reads conflict on banks.  The next chunk's TMEM load is in
-      // flight while a chunk is written out.
-      float* tile = reinterpret_cast<float*>(sout_quad);
-      uint32_t v[2][16];
-      if (have_o) {
-        tmem_ld16(tmem + lane_base + kColO, v[0]);
-        tmem_ld16(tmem + lane_base + kColO + 16, v[1]);
-      }
-#pragma unroll 1
-      for (int c0 = 0; c0 < 256; c0 += 32) {
-        float4 f[8];
-        if (have_o) {
-          tmem_ld_wait();
-          const float sc = il > 0.f ? il : 0.f;
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            f[u] = make_float4(__uint_as_float(v[u >> 2][(u & 3) * 4]) * sc,
-                               __uint_as_float(v[u >> 2][(u & 3) * 4 + 1]) * sc,
-                               __uint_as_float(v[u >> 2][(u & 3) * 4 + 2]) * sc,
-                               __uint_as_float(v[u >> 2][(u & 3) * 4 + 3]) * sc);
-          if (c0 + 32 < 256) {
-            tmem_ld16(tmem + lane_base + kColO + c0 + 32, v[0]);
-            tmem_ld16(tmem + lane_base + kColO + c0 + 48, v[1]);
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) f[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (bad) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) f[u] = make_float4(NAN, NAN, NAN, NAN);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) *reinterpret_cast<float4*>(tile + lane * 32 + ((u ^ (lane & 7)) << 2)) = f[u];
-        __syncwarp();
-        // Lane l writes column c0+l of the warp's 32 rows: one coalesced 128-byte
-        // row segment per store, addresses stepping by a constant row stride.  All
-        // 32 staged values are read first, then stored.
-        float col[32];
-#pragma unroll
-        for (int rr = 0; rr < 32; ++rr) col[rr] = tile[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
-        __syncwarp();  // the tile may be rewritten once every lane holds its column
-        const int dim = (int)cta * 256 + c0 + lane;
-        const int nr = min(32, rows_here - quad * 32);  // rows of this warp that exist
-        if (p.splits > 1) {
-          float* dst = p.partials + ((grow0 + quad * 32) * p.splits + w.split) * kPartRow + dim;
-          const int64_t step = (int64_t)p.splits * kPartRow;
-#pragma unroll
-          for (int rr = 0; rr < 32; ++rr)
-            if (rr < nr) dst[rr * step] = col[rr];
-        } else if (p.out_fp32) {
-          float* dst = reinterpret_cast<float*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
-#pragma unroll
-          for (int rr = 0; rr < 32; ++rr)
-            if (rr < nr) dst[rr * kKvLora] = col[rr];
-        } else {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
-#pragma unroll
-          for (int rr = 0; rr < 32; ++rr)
-            if (rr < nr) dst[rr * kKvLora] = __float2bfloat16_rn(col[rr]);
-        }
-      }
-      tc_fence_before();  // O read out before the next item's first PV overwrites it
-      if (!ok) break;
     }
+    tc_fence_before();
   }
-
   __syncthreads();
   cluster_sync_all();  // no remote store or arrive can target a CTA that has exited
   if (warp == 0) {
@@ -992,8 +922,14 @@ bool encode_kv_chunks(CUtensorMap* m, const void* base, uint64_t rows) {
 }  // namespace
 
 cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
-  CUtensorMap tm_kv, tm_kv3;
+  CUtensorMap tm_qn, tm_qp, tm_kv, tm_kv3;
+  const uint64_t q_rows = (uint64_t)p.batch * p.rows;
   const uint64_t kv_rows = (uint64_t)p.num_pages * kPage;
+  if (!encode_2d(&tm_qn, p.q_nope, kKvLora, q_rows, p.q_nope_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_qp, p.q_pe, kRope, q_rows, p.q_pe_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   const bool ok = p.kv_fp8 ? encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64,
                                        CU_TENSOR_MAP_SWIZZLE_NONE)
                            : encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
@@ -1002,20 +938,17 @@ cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
   // bf16 cache viewed as [chunk 0..8][row][64 columns]: row stride 1152 B, chunk stride 128 B.
   if (!p.kv_fp8 && !encode_kv_chunks(&tm_kv3, p.kv, kv_rows)) return cudaErrorInvalidValue;
   if (p.kv_fp8) tm_kv3 = tm_kv;  // unused on the FP8 path
-  // Persistent clusters: at most one per pair of SMs, each looping over items.
-  const int items = p.batch * p.splits * p.row_groups;
-  const int clusters = std::max(1, std::min(items, p.cluster_slots));
-  const dim3 grid(2 * clusters, 1, 1);
+  const dim3 grid(2 * p.row_groups, p.splits, p.batch);
   if (p.kv_fp8) {
     auto kern = split_kv_tc_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, block_threads<true>(), kSmemBytes, stream>>>(tm_kv, tm_kv3, p);
+    kern<<<grid, block_threads<true>(), kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, p);
   } else {
     auto kern = split_kv_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, block_threads<false>(), kSmemBytes, stream>>>(tm_kv, tm_kv3, p);
+    kern<<<grid, block_threads<false>(), kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, p);
   }
   return cudaGetLastError();
 }
