@@ -56,27 +56,38 @@ namespace {
 using namespace ptx;
 
 constexpr int kRows = 128;              // query rows per cluster
-constexpr int kMaxCh = 5;               // 64-column chunks a CTA holds (CTA 0: 4, CTA 1: 5)
+constexpr int kMaxCh = 5;               // FP8 cache: 64-column chunks a CTA holds (CTA 0: 4, CTA 1: 5)
 constexpr int kQChunkBytes = 128 * 128;  // 128 rows x 128 B
 constexpr int kKvChunkBytes = 64 * 128;  // 64 tokens x 128 B
-constexpr int kStageBytes = kMaxCh * kKvChunkBytes;
+constexpr int kPeHalfBytes = 64 * 64;    // 64 tokens x 32 k_pe columns (bf16 cache: 64-byte rows)
 constexpr int kStages = 4;
 constexpr int kSinQuadBytes = 32 * 32 * 4;    // peer's partial S: 32 rows x 32 tokens of one quadrant
 constexpr int kSinBytes = 4 * kSinQuadBytes;
 constexpr int kPBytes = kRows * 128;    // P[128 rows x 64 tokens] bf16
 constexpr int kPHalfBytes = kPBytes / 2;  // one token half of P
 constexpr int kStageOff = 0;
-constexpr int kQStageOff = kStageOff + 2 * kStageBytes;  // Q's c_kv chunks land in stages 2-3, then go to TMEM
-static_assert(4 * kQChunkBytes <= 2 * kStageBytes, "Q staging");
-constexpr int kSinOff = kStageOff + kStages * kStageBytes;  // S_in: the peer's partial scores, per quadrant
-constexpr int kSoutOff = kSinOff + kSinBytes;                 // S_out: partial scores staged for the peer
-constexpr int kPOff = kSoutOff + kSinBytes;                   // one P buffer
-constexpr int kQpeOff = kPOff + kPBytes;                      // CTA 1's q_pe chunk (A from shared memory)
-constexpr int kCtlOff = kQpeOff + kQChunkBytes;
 constexpr int kCtlBytes = 2048;
-constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory");
-static_assert(kPOff % 1024 == 0 && kStageOff % 1024 == 0 && kQpeOff % 1024 == 0, "swizzle atoms");
+
+// Shared-memory layout.  bf16 cache: each CTA holds four c_kv chunks and half of
+// k_pe (32 columns, 64-byte swizzled rows) of every page, so QK^T is 18 MMAs in
+// both CTAs.  FP8 cache: CTA 1 holds the whole k_pe chunk (the converter works
+// in 64-column chunks), 16 and 20 MMAs.
+template <bool kFp8>
+struct Layout {
+  static constexpr int kStageBytes = kFp8 ? kMaxCh * kKvChunkBytes : 4 * kKvChunkBytes + kPeHalfBytes;
+  static constexpr int kQStageOff = kStageOff + 2 * kStageBytes;  // Q's c_kv chunks land in stages 2-3, then go to TMEM
+  static constexpr int kSinOff = kStageOff + kStages * kStageBytes;  // S_in: the peer's partial scores, per quadrant
+  static constexpr int kSoutOff = kSinOff + kSinBytes;               // S_out: partial scores staged for the peer
+  static constexpr int kPOff = kSoutOff + kSinBytes;                 // one P buffer
+  static constexpr int kQpeOff = kPOff + kPBytes;                    // q_pe columns (A from shared memory)
+  static constexpr int kQpeBytes = kFp8 ? kQChunkBytes : kQChunkBytes / 2;
+  static constexpr int kCtlOff = kQpeOff + kQpeBytes;
+  static constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;    // + alignment slack
+  static constexpr int kRawOff = kStageBytes / 2;                    // FP8: e4m3 columns in the upper half of a stage
+  static_assert(4 * kQChunkBytes <= 2 * kStageBytes, "Q staging");
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kStageBytes % 1024 == 0 && kPOff % 1024 == 0 && kQpeOff % 1024 == 0, "swizzle atoms");
+};
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // O_c: 256 columns
@@ -89,15 +100,12 @@ template <bool kFp8>
 __host__ __device__ constexpr int pv_warp() { return kFp8 ? 10 : 6; }
 template <bool kFp8>
 __host__ __device__ constexpr int block_threads() { return 32 * (pv_warp<kFp8>() + 1); }
-constexpr int kRawOff = kStageBytes / 2;  // e4m3 columns of a page in the upper half of a stage
 constexpr int kRawBox = 64 * 64;          // one 64 tokens x 64 bytes box
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far above any legitimate wait
-constexpr int kPrefetchDist = 0;     // pages ahead pulled into L2 (0: none)
-constexpr bool kPrefetchAlt = false;  // CTAs take turns prefetching (else CTA 0 alone)  // where in a page's iteration the previous page is checked
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
@@ -202,16 +210,18 @@ template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(), 1)
     split_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
                        const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kv3,
-                       const DecodeParams p) {
+                       const __grid_constant__ CUtensorMap tm_kpe, const DecodeParams p) {
+  using Lay = Layout<kFp8>;
+  constexpr int kStageBytes = Lay::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
-  uint8_t* sQ = smem + kQStageOff;  // Q staging (then stages 2-3)
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + Lay::kCtlOff);
+  uint8_t* sQ = smem + Lay::kQStageOff;  // Q staging (then stages 2-3)
   uint8_t* sKV = smem + kStageOff;
-  uint8_t* sSin = smem + kSinOff;
-  uint8_t* sQpe = smem + kQpeOff;
-  uint8_t* sSout = smem + kSoutOff;
-  uint8_t* sP = smem + kPOff;
+  uint8_t* sSin = smem + Lay::kSinOff;
+  uint8_t* sQpe = smem + Lay::kQpeOff;
+  uint8_t* sSout = smem + Lay::kSoutOff;
+  uint8_t* sP = smem + Lay::kPOff;
 
   constexpr int kPvWarp = pv_warp<kFp8>();
   const int warp = threadIdx.x >> 5;
@@ -276,26 +286,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_pages > 0) {
-      auto pf_mine = [&](int j) { return kPrefetchAlt ? (int)cta == (j & 1) : cta == 0; };
       prefetch_tmap(&tm_kv);
-      if (!kFp8) prefetch_tmap(&tm_kv3);
-      // Optional L2 prefetch of whole upcoming pages, kPrefetchDist ahead
-      // (a page is one contiguous block of the cache).
-      const int64_t page_bytes = (int64_t)kPage * kRow * (kFp8 ? 1 : 2);
-      auto prefetch = [&](int j, int pg) {
-        if (kPrefetchDist > 0 && pf_mine(j) && pg >= 0 && pg < p.num_pages)
-          prefetch_l2(static_cast<const uint8_t*>(p.kv) + pg * page_bytes, (uint32_t)page_bytes);
-      };
-      for (int j = 0; j < kPrefetchDist && j < n_pages; ++j)
-        if (pf_mine(j)) prefetch(j, bt_row[j]);
+      if (!kFp8) {
+        prefetch_tmap(&tm_kv3);
+        prefetch_tmap(&tm_kpe);
+      }
       const int qrow = b * p.rows + row0;
-      mbar_arrive_expect_tx(&ctl->q_full, nch * kQChunkBytes);
-      for (int k = 0; k < nch; ++k) {
-        const int g = g0 + k;
-        if (g < 8)
-          tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, g * 64, qrow);
-        else
-          tma_load_2d(sQpe, &tm_qp, &ctl->q_full, 0, qrow);
+      if (kFp8) {
+        mbar_arrive_expect_tx(&ctl->q_full, nch * kQChunkBytes);
+        for (int k = 0; k < nch; ++k) {
+          const int g = g0 + k;
+          if (g < 8)
+            tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, g * 64, qrow);
+          else
+            tma_load_2d(sQpe, &tm_qp, &ctl->q_full, 0, qrow);
+        }
+      } else {  // four c_kv chunks and this CTA's 32 q_pe columns
+        mbar_arrive_expect_tx(&ctl->q_full, 4 * kQChunkBytes + kQChunkBytes / 2);
+        for (int k = 0; k < 4; ++k) tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, (g0 + k) * 64, qrow);
+        tma_load_2d(sQpe, &tm_qp, &ctl->q_full, 32 * (int)cta, qrow);
       }
       int issued = 0;
       int next_page = bt_row[0];
@@ -303,12 +312,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         const int s = j & 3;
         const int page = next_page;
         if (j + 1 < n_pages) next_page = bt_row[j + 1];  // lookups ahead of the waits
-        const int jp = j + kPrefetchDist;
-        const int pf = (kPrefetchDist > 0 && jp < n_pages && pf_mine(jp)) ? bt_row[jp] : -1;
         // Stages 2-3 hold Q until the softmax warps have moved it into TMEM.
         if (j == 2 && !wait_bar(ctl, &ctl->q_tmem, 0, p, 17)) break;
         if (!wait_bar(ctl, &ctl->empty[s], ((j >> 2) & 1) ^ 1, p, 1)) break;
-        if (pf >= 0) prefetch(jp, pf);
         uint64_t* land = kFp8 ? &ctl->raw_full[s] : &ctl->full[s];
         uint8_t* stage = sKV + s * kStageBytes;
         if (page < 0 || page >= p.num_pages) {
@@ -317,13 +323,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         } else if (kFp8) {
           mbar_arrive_expect_tx(land, nch * kRawBox);
           for (int k = 0; k < nch; ++k)
-            tma_load_2d(stage + kRawOff + k * kRawBox, &tm_kv, land, (g0 + k) * 64, page * kPage);
+            tma_load_2d(stage + Lay::kRawOff + k * kRawBox, &tm_kv, land, (g0 + k) * 64, page * kPage);
         } else {
           // The CTA's four c_kv chunks in one 3-D box (columns x rows x chunks),
-          // which lands as [chunk][row][128 B]; CTA 1's k_pe chunk in a 2-D box.
-          mbar_arrive_expect_tx(land, nch * kKvChunkBytes);
+          // which lands as [chunk][row][128 B], and its 32 k_pe columns in a 2-D
+          // box with 64-byte swizzled rows.
+          mbar_arrive_expect_tx(land, 4 * kKvChunkBytes + kPeHalfBytes);
           tma_load_3d(stage, &tm_kv3, land, 0, page * kPage, g0);
-          if (nch == 5) tma_load_2d(stage + 4 * kKvChunkBytes, &tm_kv, land, 8 * 64, page * kPage);
+          tma_load_2d(stage + 4 * kKvChunkBytes, &tm_kpe, land, 8 * 64 + 32 * (int)cta, page * kPage);
         }
         issued = j + 1;
       }
@@ -343,7 +350,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // runs ahead.
     if (lane == 0 && n_pages > 0) {
       const uint32_t kv_addr = smem_u32(sKV);
-      const uint64_t qpe_desc = sdesc_sw128(smem_u32(sQpe), 16, 1024);
+      const uint64_t qpe_desc = kFp8 ? sdesc_sw128(smem_u32(sQpe), 16, 1024) : sdesc_sw64(smem_u32(sQpe), 16, 512);
       bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
       for (int j = 0; ok && j < n_pages; ++j) {
         if (!wait_bar(ctl, &ctl->full[j & 3], (j >> 2) & 1, p, 3) ||
@@ -358,11 +365,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
             mma_bf16_ts(d, tmem + kColQ + k * 32 + kk * 8, k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4),
                         kIdescQK, (k | kk) ? 1u : 0u);
         }
-        if (nch == 5) {  // k_pe: A = q_pe from shared memory
+        if (kFp8) {
+          if (nch == 5) {  // k_pe: A = q_pe from shared memory
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4),
-                        k_desc + (uint64_t)((4 * kKvChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4),
+                          k_desc + (uint64_t)((4 * kKvChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
+          }
+        } else {  // this CTA's 32 k_pe columns: two K-steps along 64-byte swizzled rows
+          const uint64_t kpe_desc = sdesc_sw64(kv_addr + (j & 3) * kStageBytes + 4 * kKvChunkBytes, 16, 512);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+            mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4), kpe_desc + (uint64_t)((kk * 32) >> 4), kIdescQK, 1u);
         }
         mma_commit(&ctl->s_full[j & 1]);
       }
@@ -409,7 +423,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       for (int k = 0; k < 3; ++k) {
         const int u = ct + k * 128;
         if (u < units) {
-          const uint4* src = reinterpret_cast<const uint4*>(stage + kRawOff + (u >> 6) * kRawBox + (u & 63) * 64);
+          const uint4* src = reinterpret_cast<const uint4*>(stage + Lay::kRawOff + (u >> 6) * kRawBox + (u & 63) * 64);
 #pragma unroll
           for (int q = 0; q < 4; ++q) raw[k][q] = src[q];
         }
@@ -891,14 +905,15 @@ EncodeFn get_encode() {
   return fn;
 }
 
-// 2-D tensor map: `rows` rows of `cols` elements, `stride_elems` apart, box 64 x box_rows.
+// 2-D tensor map: `rows` rows of `cols` elements, `stride_elems` apart, box box_cols x box_rows.
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t stride_elems,
-               CUtensorMapDataType dt, uint32_t elem_bytes, uint32_t box_rows, CUtensorMapSwizzle swz) {
+               CUtensorMapDataType dt, uint32_t elem_bytes, uint32_t box_rows, CUtensorMapSwizzle swz,
+               uint32_t box_cols = 64) {
   EncodeFn enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {stride_elems * elem_bytes};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -922,13 +937,15 @@ bool encode_kv_chunks(CUtensorMap* m, const void* base, uint64_t rows) {
 }  // namespace
 
 cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
-  CUtensorMap tm_qn, tm_qp, tm_kv, tm_kv3;
+  CUtensorMap tm_qn, tm_qp, tm_kv, tm_kv3, tm_kpe;
   const uint64_t q_rows = (uint64_t)p.batch * p.rows;
   const uint64_t kv_rows = (uint64_t)p.num_pages * kPage;
   if (!encode_2d(&tm_qn, p.q_nope, kKvLora, q_rows, p.q_nope_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tm_qp, p.q_pe, kRope, q_rows, p.q_pe_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+      !(p.kv_fp8 ? encode_2d(&tm_qp, p.q_pe, kRope, q_rows, p.q_pe_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                             128, CU_TENSOR_MAP_SWIZZLE_128B)
+                 : encode_2d(&tm_qp, p.q_pe, kRope, q_rows, p.q_pe_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                             128, CU_TENSOR_MAP_SWIZZLE_64B, 32)))
     return cudaErrorInvalidValue;
   const bool ok = p.kv_fp8 ? encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64,
                                        CU_TENSOR_MAP_SWIZZLE_NONE)
@@ -937,18 +954,24 @@ cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
   if (!ok) return cudaErrorInvalidValue;
   // bf16 cache viewed as [chunk 0..8][row][64 columns]: row stride 1152 B, chunk stride 128 B.
   if (!p.kv_fp8 && !encode_kv_chunks(&tm_kv3, p.kv, kv_rows)) return cudaErrorInvalidValue;
-  if (p.kv_fp8) tm_kv3 = tm_kv;  // unused on the FP8 path
+  // bf16 cache: 32 k_pe columns per box, 64-byte swizzled rows.
+  if (!p.kv_fp8 && !encode_2d(&tm_kpe, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
+                              CU_TENSOR_MAP_SWIZZLE_64B, 32))
+    return cudaErrorInvalidValue;
+  if (p.kv_fp8) tm_kv3 = tm_kpe = tm_kv;  // unused on the FP8 path
   const dim3 grid(2 * p.row_groups, p.splits, p.batch);
   if (p.kv_fp8) {
     auto kern = split_kv_tc_kernel<true>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    constexpr int kSmem = Layout<true>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, block_threads<true>(), kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, p);
+    kern<<<grid, block_threads<true>(), kSmem, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, tm_kpe, p);
   } else {
     auto kern = split_kv_tc_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    constexpr int kSmem = Layout<false>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, block_threads<false>(), kSmemBytes, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, p);
+    kern<<<grid, block_threads<false>(), kSmem, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, tm_kpe, p);
   }
   return cudaGetLastError();
 }

@@ -315,6 +315,13 @@ __device__ __forceinline__ uint64_t sdesc_noswz(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46);
 }
 
+// Shared-memory matrix descriptor, 64-byte swizzle (layout 4): K-major rows of
+// 64 bytes; sbo = byte distance between 8-row groups (512 for packed rows).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
+         ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (4ull << 61);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4,
 //   32-45 stride byte offset >> 4, 46-48 fixed 0b001, 61-63 layout (2 = 128B swizzle).
