@@ -328,6 +328,14 @@ def main():
     achieved_gbs = abytes / (split_us * 1e-6) / 1e9
     achieved_tf = aflops / (split_us * 1e-6) / 1e12
     traffic = recorded_traffic(name)
+    # The binding roofline is the one with the longer floor for this workload:
+    # HBM for few query rows per page, the tensor pipe for many (e.g. 256 rows).
+    hbm = {"achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": achieved_gbs / hbm_peak}
+    tc = {"achieved": achieved_tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved_tf / tc_peak}
+    if aflops / (tc_peak * 1e12) > abytes / (hbm_peak * 1e9):
+        roofline = {"bound": "tensor", **tc, "traffic": traffic, "peak_source": peak_kind, "hbm": hbm}
+    else:
+        roofline = {"bound": "hbm", **hbm, "traffic": traffic, "peak_source": peak_kind, "tensor": tc}
 
     line = {
         "metric": METRIC, "value": step_us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -343,11 +351,7 @@ def main():
         "gb_per_s": abytes * world / (step_us * 1e-6) / 1e9,
         "tflops": aflops * world / (step_us * 1e-6) / 1e12,
         "kernel_us": {"split_kv": split_us, "combine": comb_us},
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm_peak, "traffic": traffic,
-                     "peak_source": peak_kind,
-                     "tensor": {"achieved": achieved_tf, "peak": tc_peak, "unit": "TFLOP/s",
-                                "frac": achieved_tf / tc_peak}},
+        "roofline": roofline,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * (1 + (pl.num_kv_splits > 1)),
         "clocks": clk,

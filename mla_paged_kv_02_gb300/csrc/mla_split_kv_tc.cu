@@ -7,9 +7,11 @@
 // "one KV read per tile for all heads and MTP rows" reading of the TokenSpeed
 // MLA summary's sub-linear KV scan claim, vLLM PR #41778, motivation).
 //
-// The 576-wide contraction is split between the two CTAs: CTA 0 holds columns
-// [0, 256) of Q and of every page, CTA 1 holds [256, 576) (the rest of c_kv and
-// k_pe).  That keeps both operands of every MMA at 128 rows:
+// The 576-wide contraction is split between the two CTAs: CTA c holds c_kv
+// columns [256c, 256c+256) of Q and of every page, and with a bf16 cache k_pe
+// columns [32c, 32c+32) (with an FP8 cache CTA 1 holds all 64, since the
+// converter works in 64-column chunks).  That keeps both operands of every MMA
+// at 128 rows:
 //   QK^T : S_c[128 rows x 64 tok] = Q[:, cols_c] . K[:, cols_c]^T  (M=128, N=64)
 //   PV   : O_c[128 rows x 256]   += P[128 x 64] . V[64 x cols_c(256)] (M=128, N=256)
 // where each CTA's 256 V columns are exactly the first four 64-column chunks it
@@ -24,8 +26,10 @@
 //
 // Warp roles (224 threads; 352 for an FP8 cache):
 //   warp 0     TMA producer: Q once, then per page a block-table lookup and the
-//              CTA's 4 or 5 64x64 boxes (128B swizzle) into a 4-stage ring; owns
-//              the TMEM allocation.
+//              CTA's columns of the page into a 4-stage ring (bf16: one 3-D box
+//              of four 64x64 chunks, 128B swizzle, and one 32-column k_pe box,
+//              64B swizzle; FP8: 4 or 5 boxes of 64x64 bytes); owns the TMEM
+//              allocation.
 //   warp 1     QK^T issuer (one thread).
 //   warps 2-5  softmax / exchange / epilogue warpgroup.  Warp w reads TMEM lane
 //              quadrant w%4 (rows 32*(w%4) .. +31) and works on its CTA's token
@@ -41,7 +45,7 @@
 //
 // Q's c_kv columns are kept in tensor memory as the A operand of QK^T (read every
 // page; from TMEM they cost no shared-memory bandwidth and leave room for 4 page
-// stages); CTA 1's q_pe chunk stays in shared memory.
+// stages); the CTA's q_pe columns stay in shared memory.
 // TMEM: O_c at columns [0,256), S double buffer at [256,384), Q at [384,512).
 #include <cuda_fp8.h>
 
@@ -78,8 +82,9 @@ struct Layout {
   static constexpr int kQStageOff = kStageOff + 2 * kStageBytes;  // Q's c_kv chunks land in stages 2-3, then go to TMEM
   static constexpr int kSinOff = kStageOff + kStages * kStageBytes;  // S_in: the peer's partial scores, per quadrant
   static constexpr int kSoutOff = kSinOff + kSinBytes;               // S_out: partial scores staged for the peer
-  static constexpr int kPOff = kSoutOff + kSinBytes;                 // one P buffer
-  static constexpr int kQpeOff = kPOff + kPBytes;                    // q_pe columns (A from shared memory)
+  static constexpr int kPBufs = kFp8 ? 1 : 2;                        // P buffers (FP8: no room for two)
+  static constexpr int kPOff = kSoutOff + kSinBytes;
+  static constexpr int kQpeOff = kPOff + kPBufs * kPBytes;           // q_pe columns (A from shared memory)
   static constexpr int kQpeBytes = kFp8 ? kQChunkBytes : kQChunkBytes / 2;
   static constexpr int kCtlOff = kQpeOff + kQpeBytes;
   static constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;    // + alignment slack
@@ -126,7 +131,7 @@ struct Ctl {
   uint64_t s_free[2];          // the 4 softmax warps have read it (count 4)
   uint64_t sin_full[4];        // per quadrant: the peer's partial S landed (count 1 + 4 KB of st.async bytes)
   uint64_t sin_free[4];        // per quadrant: the peer consumed what this CTA sent (count 1, remote)
-  uint64_t p_free;             // PV of the previous page done in both CTAs: P rewritable (count 2)
+  uint64_t p_free[2];          // PV done in both CTAs: that P buffer rewritable (count 2)
   uint64_t pv_ready[2];        // local P halves written (count 4) + the peer's halves landed
   uint64_t u_ready[2];         // the peer's references for the page landed (count 4 + 512 B)
   uint64_t checked[2];         // the 4 local warps ran the page's reference check (count 4)
@@ -265,7 +270,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       mbar_init(&ctl->checked[e], 4);
       mbar_init(&ctl->u_ready[e], 4);
     }
-    mbar_init(&ctl->p_free, 2);
+    mbar_init(&ctl->p_free[0], 2);
+    mbar_init(&ctl->p_free[1], 2);
     mbar_init(&ctl->fin, 4);
     mbar_init(&ctl->drain, 2);  // both MMA-issuing threads' last commits
     ctl->abort = 0;
@@ -397,13 +403,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
             !wait_bar(ctl, &ctl->checked[j & 1], (j >> 1) & 1, p, 7))
           break;
         tc_fence_after();
+        const int pb = j % Lay::kPBufs;
         const uint64_t v_desc = sdesc_sw128(kv_addr + (j & 3) * kStageBytes, kKvChunkBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // A = P tokens 16kk..16kk+15: two 8-token chunks of one half
-          mma_bf16_ss(tmem + kColO, sdesc_noswz(p_addr + (kk >> 1) * kPHalfBytes + ((2 * kk) & 3) * 128, 128, 512),
+          mma_bf16_ss(tmem + kColO,
+                      sdesc_noswz(p_addr + pb * kPBytes + (kk >> 1) * kPHalfBytes + ((2 * kk) & 3) * 128, 128, 512),
                       v_desc + (uint64_t)((kk * 2048) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&ctl->empty[j & 3]);      // stage free; O current through page j
-        mma_commit_multicast(&ctl->p_free, 3);  // P reusable, in both CTAs
+        mma_commit(&ctl->empty[j & 3]);           // stage free; O current through page j
+        mma_commit_multicast(&ctl->p_free[pb], 3);  // P buffer reusable, in both CTAs
       }
       mma_commit(&ctl->drain);
       const uint64_t t0 = globaltimer_ns();
@@ -459,7 +467,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // for all 128 rows; warp w handles the rows of TMEM lane quadrant w%4.  Per
     // page a warp hands the peer the partial scores of the peer's token half,
     // adds the peer's partial for its own half, and computes P for its half, which
-    // it writes into both CTAs' P buffers.
+    // it writes into both CTAs' P buffers.  Order within page j: add the peer's
+    // partial of S(j); settle and send the reference; P(j) out; S(j+1) out; check
+    // page j.  P(j) leaves before S(j+1) is taken so that PV(j), and with it the
+    // release of page j's stage for the next load, is not held up by the exchange.
     //
     // Reference maxima.  P of one row must share one reference across both
     // halves, yet neither CTA sees the other's scores.  Each CTA computes with
@@ -491,17 +502,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     float r_ref = -INFINITY;   // reference this CTA computes P with
     float a_ref = -INFINITY;   // reference both CTAs agreed on, through the last checked page
     float l_sum = 0.f;         // exp sum over this CTA's token halves, relative to r_ref
-    float u_prev = -INFINITY;  // reference the previous page was computed with
     bool poisoned = !len_ok;
     bool ok = true;
 
     // 16-byte chunk u (tokens 8u..8u+7) of this thread's row of P.  P is K-major
     // without swizzle, laid out [token half][8-row group][8-token chunk][row][16 B],
     // so a warp's 32 rows of one token half are 2 KB of contiguous bytes.
-    auto p_chunk = [&](int u) -> uint8_t* {
-      return sP + (u >> 2) * kPHalfBytes + (r >> 3) * 512 + (u & 3) * 128 + (r & 7) * 16;
+    auto p_chunk = [&](int pb, int u) -> uint8_t* {
+      return sP + pb * kPBytes + (u >> 2) * kPHalfBytes + (r >> 3) * 512 + (u & 3) * 128 + (r & 7) * 16;
     };
-    uint8_t* p_mine = sP + (int)cta * kPHalfBytes + quad * 2048;  // this warp's rows of this CTA's half
+    const int p_mine_off = (int)cta * kPHalfBytes + quad * 2048;  // this warp's rows of this CTA's half
 
     // S(jj) from TMEM: this CTA's token half stays in `own`; the peer's half is
     // staged in S_out and goes to the peer's S_in for this quadrant as one 4 KB
@@ -575,7 +585,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
             const float f = ex2((h == (int)cta ? u_own : u_oth) - an);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              uint4* c = reinterpret_cast<uint4*>(p_chunk(4 * h + u));
+              uint4* c = reinterpret_cast<uint4*>(p_chunk(k % Lay::kPBufs, 4 * h + u));
               uint4 w = *c;
               uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
@@ -690,14 +700,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       __syncwarp();  // every lane's S_in values are in registers
       if (lane == 0) mbar_arrive_cluster_relaxed(sin_free_peer);
 
-      // The previous page's references are checked (PV(j-1), and with it the
-      // release of its stage, waits for this), then this page's reference is
-      // settled and goes to the peer first, ahead of the larger transfers, so
-      // that the peer's check of this page need not wait for them.
-      if (j >= 1 && !check(j - 1, u_prev)) {
-        ok = false;
-        break;
-      }
+      // This page's reference is settled and goes to the peer first, ahead of
+      // the larger transfers, so that the peer's check of this page need not
+      // wait for them.
       if (mx > r_ref + kRescaleThreshold) {  // false while every column is masked
         const float u = ceilf(mx);
         l_sum *= ex2(r_ref - u);
@@ -708,11 +713,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
                    mapa_shared(smem_u32(&ctl->u_ready[e]), peer));
       if (lane == 0) mbar_arrive_expect_tx(&ctl->u_ready[e], kUReadyTx);
 
-      // Next page's scores to the peer while this page's P is computed.
-      if (j + 1 < n_pages && !take_s(j + 1, sv_next)) {
-        ok = false;
-        break;
-      }
 
       // V rows of tokens at or past L (or of a page that was never loaded) may
       // hold anything, NaN included; zero this CTA's 256 V columns of them.
@@ -766,25 +766,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       }
       l_sum += (part[0] + part[1]) + (part[2] + part[3]);
 
-      // Both CTAs' PV of page j-1 must be done before P is rewritten.
-      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->p_free, (j & 1) ^ 1, p, 15))) {
+      // Both CTAs' PV of the page that last used this P buffer must be done.
+      const int pb = j % Lay::kPBufs;
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->p_free[pb], ((j / Lay::kPBufs) & 1) ^ 1, p, 15))) {
         ok = false;
         break;
       }
       // The warp's P rows go to the peer as one 2 KB bulk copy (the copy engine
       // carries them; the warp does not stall on the pair's link).
 #pragma unroll
-      for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(p_chunk(4 * (int)cta + u)) = pk[u];
+      for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(p_chunk(pb, 4 * (int)cta + u)) = pk[u];
       fence_proxy_async_smem();  // P rows (and any zeroed V rows) visible to the MMA and the copy engine
       __syncwarp();
       const uint32_t pv_bar_peer = mapa_shared(smem_u32(&ctl->pv_ready[e]), peer);
       if (lane == 0) {
         mbar_arrive_expect_tx(&ctl->pv_ready[e], kPvReadyTx);
-        bulk_copy_to_peer(p_peer + (uint32_t)(p_mine - sP), p_mine, 2048, pv_bar_peer);
+        const int off = pb * kPBytes + p_mine_off;
+        bulk_copy_to_peer(p_peer + (uint32_t)off, sP + off, 2048, pv_bar_peer);
       }
-      u_prev = u_cur;
+      // Then the next page's scores to the peer, and this page's reference
+      // check, after which PV(j) may go as soon as the peer's P is in.
+      if (j + 1 < n_pages && !take_s(j + 1, sv_next)) {
+        ok = false;
+        break;
+      }
+      if (!check(j, u_cur)) {
+        ok = false;
+        break;
+      }
     }
-    if (ok && n_pages >= 1 && !check(n_pages - 1, u_prev)) ok = false;
     ok = !wg_sync_or(!ok);  // the epilogue decides as one group
 
     // ------------------------------------------------------------ epilogue
