@@ -24,7 +24,7 @@
 // maxima and row sums go by st.async.  Both complete transaction bytes on the
 // receiver's mbarrier.
 //
-// Warp roles (224 threads; 352 for an FP8 cache):
+// Warp roles (352 threads):
 //   warp 0     TMA producer: Q once, then per page a block-table lookup and the
 //              CTA's columns of the page into a 4-stage ring (bf16: one 3-D box
 //              of four 64x64 chunks, 128B swizzle, and one 32-column k_pe box,
@@ -36,12 +36,14 @@
 //              half of those rows.  Online softmax in the exp2 domain with lazily
 //              raised whole-number reference maxima, agreed between the pair one
 //              page behind (see the warpgroup's comment).
+//   warps 6-9  (bf16 cache) S senders: the peer's token half of S(j) from TMEM
+//              to the peer, off the softmax warps' chain.
 //   warps 6-9  (FP8 cache) converter: the CTA's e4m3 columns land in the upper
 //              half of a stage; every thread first pulls its share into
 //              registers, then writes exact bf16 values (e4m3 is a subset of
 //              bf16) in the swizzled layout.  The per-tensor scale is folded into
 //              the softmax scale and the epilogue.
-//   warp 6/10  PV issuer (one thread; warp 10 with an FP8 cache).
+//   warp 10    PV issuer (one thread).
 //
 // Q's c_kv columns are kept in tensor memory as the A operand of QK^T (read every
 // page; from TMEM they cost no shared-memory bandwidth and leave room for 4 page
@@ -101,8 +103,9 @@ constexpr uint32_t kColQ = 384;  // Q's c_kv chunks as the A operand: 2 bf16 per
 
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kConvWarp0 = 6;    // FP8 converter warps 6-9
+constexpr int kSendWarp0 = 6;    // bf16 cache: S sender warps 6-9
 template <bool kFp8>
-__host__ __device__ constexpr int pv_warp() { return kFp8 ? 10 : 6; }
+__host__ __device__ constexpr int pv_warp() { return 10; }
 template <bool kFp8>
 __host__ __device__ constexpr int block_threads() { return 32 * (pv_warp<kFp8>() + 1); }
 constexpr int kRawBox = 64 * 64;          // one 64 tokens x 64 bytes box
@@ -259,8 +262,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     mbar_init(&ctl->q_tmem, 4);
     mbar_init(&ctl->s_full[0], 1);
     mbar_init(&ctl->s_full[1], 1);
-    mbar_init(&ctl->s_free[0], 4);
-    mbar_init(&ctl->s_free[1], 4);
+    mbar_init(&ctl->s_free[0], kFp8 ? 4 : 8);  // softmax warps (+ sender warps)
+    mbar_init(&ctl->s_free[1], kFp8 ? 4 : 8);
     for (int q = 0; q < 4; ++q) {
       mbar_init(&ctl->sin_full[q], 1);
       mbar_init(&ctl->sin_free[q], 1);
@@ -461,6 +464,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       conv_sync();
       if (lane == 0) mbar_arrive(&ctl->full[s]);
     }
+  } else if (!kFp8 && warp >= kSendWarp0 && warp < kSendWarp0 + 4) {
+    // ------------------------------------------------------------ S sender (bf16 cache)
+    // The peer's token half of S(j), for the rows of TMEM lane quadrant w%4, goes
+    // from TMEM through S_out to the peer's S_in as one 4 KB bulk copy, as soon as
+    // QK(j) is done and the peer has consumed the previous page's partial (which
+    // also means the previous copy has read S_out).  Off the softmax warps' chain,
+    // the peer's partial is in place before the softmax warps come to it.
+    const int quad = warp & 3;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t col_oth = kColS + 32 * peer;
+    uint8_t* sout_quad = sSout + quad * kSinQuadBytes;
+    uint8_t* sout_row = sout_quad + lane * 128;
+    const uint32_t sin_quad_peer = mapa_shared(smem_u32(sSin + quad * kSinQuadBytes), peer);
+    const uint32_t sin_full_peer = mapa_shared(smem_u32(&ctl->sin_full[quad]), peer);
+    for (int j = 0; j < n_pages; ++j) {
+      const int sb = j & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[sb], (j >> 1) & 1, p, 20))) break;
+      tc_fence_after();
+      uint32_t oth[2][16];
+      tmem_ld16(tmem + lane_base + col_oth + sb * 64, oth[0]);
+      tmem_ld16(tmem + lane_base + col_oth + sb * 64 + 16, oth[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
+      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_free[quad], (j & 1) ^ 1, p, 13))) break;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(sout_row + ((u ^ (lane & 7)) << 4)) =
+            make_uint4(oth[u >> 2][(u & 3) * 4], oth[u >> 2][(u & 3) * 4 + 1], oth[u >> 2][(u & 3) * 4 + 2],
+                       oth[u >> 2][(u & 3) * 4 + 3]);
+      fence_proxy_async_smem();  // staged rows visible to the copy engine
+      __syncwarp();
+      if (lane == 0) bulk_copy_to_peer(sin_quad_peer, sout_quad, kSinQuadBytes, sin_full_peer);
+    }
   } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
     // ------------------------------------------------------------ softmax / exchange warpgroup
     // Each CTA owns one half of every page's 64 tokens (CTA c: tokens 32c..32c+31)
@@ -513,11 +551,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     };
     const int p_mine_off = (int)cta * kPHalfBytes + quad * 2048;  // this warp's rows of this CTA's half
 
-    // S(jj) from TMEM: this CTA's token half stays in `own`; the peer's half is
-    // staged in S_out and goes to the peer's S_in for this quadrant as one 4 KB
-    // bulk copy, once the peer has consumed the previous page's (which also means
-    // the previous copy has read S_out).  The copy engine carries the bytes, so
-    // the warp does not stall on the pair's link.
+    // S(jj) from TMEM: this CTA's token half goes to `own`.  The peer's half goes
+    // to the peer's S_in for this quadrant as one 4 KB bulk copy, staged in S_out:
+    // with a bf16 cache the sender warps do that, with an FP8 cache (no room for
+    // more warps) this warp does, once the peer has consumed the previous page's
+    // (which also means the previous copy has read S_out).  The copy engine
+    // carries the bytes, so no warp stalls on the pair's link.
     auto take_s = [&](int jj, float (&own)[32]) -> bool {
       const int sb = jj & 1;
       if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[sb], (jj >> 1) & 1, p, 6))) return false;
@@ -525,14 +564,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       uint32_t mine[2][16], oth[2][16];
       tmem_ld16(tmem + lane_base + col_own + sb * 64, mine[0]);
       tmem_ld16(tmem + lane_base + col_own + sb * 64 + 16, mine[1]);
-      tmem_ld16(tmem + lane_base + col_oth + sb * 64, oth[0]);
-      tmem_ld16(tmem + lane_base + col_oth + sb * 64 + 16, oth[1]);
+      if (kFp8) {
+        tmem_ld16(tmem + lane_base + col_oth + sb * 64, oth[0]);
+        tmem_ld16(tmem + lane_base + col_oth + sb * 64 + 16, oth[1]);
+      }
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
 #pragma unroll
       for (int k = 0; k < 32; ++k) own[k] = __uint_as_float(mine[k >> 4][k & 15]);
+      if (!kFp8) return true;
       if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_free[quad], (jj & 1) ^ 1, p, 13))) return false;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
