@@ -66,7 +66,7 @@ constexpr int kMaxCh = 5;               // FP8 cache: 64-column chunks a CTA hol
 constexpr int kQChunkBytes = 128 * 128;  // 128 rows x 128 B
 constexpr int kKvChunkBytes = 64 * 128;  // 64 tokens x 128 B
 constexpr int kPeHalfBytes = 64 * 64;    // 64 tokens x 32 k_pe columns (bf16 cache: 64-byte rows)
-constexpr int kStages = 4;
+constexpr int kMaxStages = 5;  // page stages in the ring (at most)
 constexpr int kSinQuadBytes = 32 * 32 * 4;    // peer's partial S: 32 rows x 32 tokens of one quadrant
 constexpr int kSinBytes = 4 * kSinQuadBytes;
 constexpr int kPBytes = kRows * 128;    // P[128 rows x 64 tokens] bf16
@@ -81,7 +81,9 @@ constexpr int kCtlBytes = 2048;
 template <bool kFp8>
 struct Layout {
   static constexpr int kStageBytes = kFp8 ? kMaxCh * kKvChunkBytes : 4 * kKvChunkBytes + kPeHalfBytes;
-  static constexpr int kQStageOff = kStageOff + 2 * kStageBytes;  // Q's c_kv chunks land in stages 2-3, then go to TMEM
+  static constexpr int kStages = 4;                                  // page stages in the ring
+  // Q's c_kv chunks land in the last two stages' space, then go to TMEM.
+  static constexpr int kQStageOff = kStageOff + (kStages - 2) * kStageBytes;
   static constexpr int kSinOff = kStageOff + kStages * kStageBytes;  // S_in: the peer's partial scores, per quadrant
   static constexpr int kSoutOff = kSinOff + kSinBytes;               // S_out: partial scores staged for the peer
   static constexpr int kPBufs = kFp8 ? 1 : 2;                        // P buffers (FP8: no room for two)
@@ -92,6 +94,7 @@ struct Layout {
   static constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;    // + alignment slack
   static constexpr int kRawOff = kStageBytes / 2;                    // FP8: e4m3 columns in the upper half of a stage
   static_assert(4 * kQChunkBytes <= 2 * kStageBytes, "Q staging");
+  static_assert(kStages >= 3 && kStages <= kMaxStages, "stages");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kStageBytes % 1024 == 0 && kPOff % 1024 == 0 && kQpeOff % 1024 == 0, "swizzle atoms");
 };
@@ -126,9 +129,9 @@ constexpr uint32_t kUReadyTx = 32 * 4;
 
 struct Ctl {
   uint64_t q_full;
-  uint64_t raw_full[kStages];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];     // this CTA's PV of the stage's page has completed
+  uint64_t raw_full[kMaxStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];     // this CTA's PV of the stage's page has completed
   uint64_t q_tmem;             // Q moved from shared to tensor memory (count 4)
   uint64_t s_full[2];          // QK^T of the page is in TMEM
   uint64_t s_free[2];          // the 4 softmax warps have read it (count 4)
@@ -221,6 +224,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
                        const __grid_constant__ CUtensorMap tm_kpe, const DecodeParams p) {
   using Lay = Layout<kFp8>;
   constexpr int kStageBytes = Lay::kStageBytes;
+  constexpr int kNS = Lay::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + Lay::kCtlOff);
@@ -254,7 +258,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kNS; ++s) {
       mbar_init(&ctl->raw_full[s], 1);
       mbar_init(&ctl->full[s], kFp8 ? 4 : 1);
       mbar_init(&ctl->empty[s], 1);
@@ -318,12 +322,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       int issued = 0;
       int next_page = bt_row[0];
       for (int j = 0; j < n_pages; ++j) {
-        const int s = j & 3;
+        const int s = j % kNS;
         const int page = next_page;
         if (j + 1 < n_pages) next_page = bt_row[j + 1];  // lookups ahead of the waits
-        // Stages 2-3 hold Q until the softmax warps have moved it into TMEM.
-        if (j == 2 && !wait_bar(ctl, &ctl->q_tmem, 0, p, 17)) break;
-        if (!wait_bar(ctl, &ctl->empty[s], ((j >> 2) & 1) ^ 1, p, 1)) break;
+        // The last two stages hold Q until the softmax warps have moved it into TMEM.
+        if (j == kNS - 2 && !wait_bar(ctl, &ctl->q_tmem, 0, p, 17)) break;
+        if (!wait_bar(ctl, &ctl->empty[s], ((j / kNS) & 1) ^ 1, p, 1)) break;
         uint64_t* land = kFp8 ? &ctl->raw_full[s] : &ctl->full[s];
         uint8_t* stage = sKV + s * kStageBytes;
         if (page < 0 || page >= p.num_pages) {
@@ -344,10 +348,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         issued = j + 1;
       }
       // Never leave with copies in flight.
-      for (int j = max(0, issued - kStages); j < issued; ++j) {
-        uint64_t* land = kFp8 ? &ctl->raw_full[j & 3] : &ctl->full[j & 3];
+      for (int j = max(0, issued - kNS); j < issued; ++j) {
+        uint64_t* land = kFp8 ? &ctl->raw_full[j % kNS] : &ctl->full[j % kNS];
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(land), (j >> 2) & 1))
+        while (!mbar_try_wait(smem_u32(land), (j / kNS) & 1))
           if (globaltimer_ns() - t0 > kWaitLimitNs) break;
       }
     }
@@ -362,11 +366,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       const uint64_t qpe_desc = kFp8 ? sdesc_sw128(smem_u32(sQpe), 16, 1024) : sdesc_sw64(smem_u32(sQpe), 16, 512);
       bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
       for (int j = 0; ok && j < n_pages; ++j) {
-        if (!wait_bar(ctl, &ctl->full[j & 3], (j >> 2) & 1, p, 3) ||
+        if (!wait_bar(ctl, &ctl->full[j % kNS], (j / kNS) & 1, p, 3) ||
             !wait_bar(ctl, &ctl->s_free[j & 1], ((j >> 1) & 1) ^ 1, p, 4))
           break;
         tc_fence_after();
-        const uint64_t k_desc = sdesc_sw128(kv_addr + (j & 3) * kStageBytes, 16, 1024);
+        const uint64_t k_desc = sdesc_sw128(kv_addr + (j % kNS) * kStageBytes, 16, 1024);
         const uint32_t d = tmem + kColS + (j & 1) * 64;
         for (int k = 0; k < 4; ++k) {
 #pragma unroll
@@ -382,7 +386,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
                           k_desc + (uint64_t)((4 * kKvChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
           }
         } else {  // this CTA's 32 k_pe columns: two K-steps along 64-byte swizzled rows
-          const uint64_t kpe_desc = sdesc_sw64(kv_addr + (j & 3) * kStageBytes + 4 * kKvChunkBytes, 16, 512);
+          const uint64_t kpe_desc = sdesc_sw64(kv_addr + (j % kNS) * kStageBytes + 4 * kKvChunkBytes, 16, 512);
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
             mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4), kpe_desc + (uint64_t)((kk * 32) >> 4), kIdescQK, 1u);
@@ -407,13 +411,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
           break;
         tc_fence_after();
         const int pb = j % Lay::kPBufs;
-        const uint64_t v_desc = sdesc_sw128(kv_addr + (j & 3) * kStageBytes, kKvChunkBytes, 1024);
+        const uint64_t v_desc = sdesc_sw128(kv_addr + (j % kNS) * kStageBytes, kKvChunkBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // A = P tokens 16kk..16kk+15: two 8-token chunks of one half
           mma_bf16_ss(tmem + kColO,
                       sdesc_noswz(p_addr + pb * kPBytes + (kk >> 1) * kPHalfBytes + ((2 * kk) & 3) * 128, 128, 512),
                       v_desc + (uint64_t)((kk * 2048) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&ctl->empty[j & 3]);           // stage free; O current through page j
+        mma_commit(&ctl->empty[j % kNS]);           // stage free; O current through page j
         mma_commit_multicast(&ctl->p_free[pb], 3);  // P buffer reusable, in both CTAs
       }
       mma_commit(&ctl->drain);
@@ -426,8 +430,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
     const int units = nch * 64;                    // (chunk, token) pairs of 64 bytes
     for (int j = 0; j < n_pages; ++j) {
-      const int s = j & 3;
-      if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[s], (j >> 2) & 1, p, 9))) break;
+      const int s = j % kNS;
+      if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[s], (j / kNS) & 1, p, 9))) break;
       uint8_t* stage = sKV + s * kStageBytes;
       uint4 raw[3][4];
 #pragma unroll
@@ -602,7 +606,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         if (__any_sync(0xffffffffu, resc)) {
           // O holds exactly pages < k once PV(k-1) has completed.
           if (!__all_sync(0xffffffffu,
-                          wait_bar(ctl, &ctl->empty[(k - 1) & 3], ((k - 1) >> 2) & 1, p, 12)))
+                          wait_bar(ctl, &ctl->empty[(k - 1) % kNS], ((k - 1) / kNS) & 1, p, 12)))
             return false;
           tc_fence_after();
           const float f = resc ? ex2(a_ref - an) : 1.f;
@@ -763,7 +767,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       if (n_valid < kPage) {
         const int t = r >> 1;
         if (t >= n_valid) {
-          uint8_t* stage = sKV + (j & 3) * kStageBytes;
+          uint8_t* stage = sKV + (j % kNS) * kStageBytes;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint4* rowp = reinterpret_cast<uint4*>(stage + ((r & 1) * 2 + c) * kKvChunkBytes + t * 128);
@@ -846,7 +850,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     if (lane == 0) mbar_arrive_expect_tx(&ctl->fin, 32 * 4);
     if (poisoned) atomicOr(&ctl->poisoned, 1);
     bool fail = !wait_bar(ctl, &ctl->fin, 0, p, 16);
-    fail |= !ok || (n_pages > 0 && !wait_bar(ctl, &ctl->empty[(n_pages - 1) & 3], ((n_pages - 1) >> 2) & 1, p, 8));
+    fail |= !ok || (n_pages > 0 && !wait_bar(ctl, &ctl->empty[(n_pages - 1) % kNS], ((n_pages - 1) / kNS) & 1, p, 8));
     fail = wg_sync_or(fail);
     tc_fence_after();
     __syncwarp();
