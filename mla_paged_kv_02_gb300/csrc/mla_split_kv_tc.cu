@@ -400,23 +400,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     }
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV issuer
-    // PV(j) once both CTAs' P halves of page j are in and the local warps have
-    // checked its references (and scaled O or P where they moved).
+    // PV(j) in two halves of 32 tokens: this CTA's own half as soon as the local
+    // warps have checked page j's references (which they do after writing their
+    // P rows, scaling O or P where the references moved), the peer's half once
+    // its P rows have landed.  The own half runs while the peer's are in flight.
     if (lane == 0 && n_pages > 0) {
       const uint32_t kv_addr = smem_u32(sKV);
       const uint32_t p_addr = smem_u32(sP);
-      for (int j = 0; j < n_pages; ++j) {
-        if (!wait_bar(ctl, &ctl->pv_ready[j & 1], (j >> 1) & 1, p, 5) ||
-            !wait_bar(ctl, &ctl->checked[j & 1], (j >> 1) & 1, p, 7))
-          break;
+      bool ok = true;
+      for (int j = 0; ok && j < n_pages; ++j) {
+        if (!wait_bar(ctl, &ctl->checked[j & 1], (j >> 1) & 1, p, 7)) break;
         tc_fence_after();
         const int pb = j % Lay::kPBufs;
         const uint64_t v_desc = sdesc_sw128(kv_addr + (j % kNS) * kStageBytes, kKvChunkBytes, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // A = P tokens 16kk..16kk+15: two 8-token chunks of one half
-          mma_bf16_ss(tmem + kColO,
-                      sdesc_noswz(p_addr + pb * kPBytes + (kk >> 1) * kPHalfBytes + ((2 * kk) & 3) * 128, 128, 512),
-                      v_desc + (uint64_t)((kk * 2048) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int i = 0; i < 2; ++i) {
+          const int h = i == 0 ? (int)cta : (int)peer;  // token half
+          if (i == 1) {
+            if (!wait_bar(ctl, &ctl->pv_ready[j & 1], (j >> 1) & 1, p, 5)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {  // A = P tokens 16kk..16kk+15: two 8-token chunks of half h
+            const int kk = 2 * h + t;
+            mma_bf16_ss(tmem + kColO,
+                        sdesc_noswz(p_addr + pb * kPBytes + h * kPHalfBytes + ((2 * kk) & 3) * 128, 128, 512),
+                        v_desc + (uint64_t)((kk * 2048) >> 4), kIdescPV, (j > 0 || i > 0 || t > 0) ? 1u : 0u);
+          }
+        }
+        if (!ok) break;
         mma_commit(&ctl->empty[j % kNS]);           // stage free; O current through page j
         mma_commit_multicast(&ctl->p_free[pb], 3);  // P buffer reusable, in both CTAs
       }
