@@ -8,10 +8,8 @@
 // MLA summary's sub-linear KV scan claim, vLLM PR #41778, motivation).
 //
 // The 576-wide contraction is split between the two CTAs: CTA c holds c_kv
-// columns [256c, 256c+256) of Q and of every page, and with a bf16 cache k_pe
-// columns [32c, 32c+32) (with an FP8 cache CTA 1 holds all 64, since the
-// converter works in 64-column chunks).  That keeps both operands of every MMA
-// at 128 rows:
+// columns [256c, 256c+256) and k_pe columns [32c, 32c+32) of Q and of every
+// page.  That keeps both operands of every MMA at 128 rows:
 //   QK^T : S_c[128 rows x 64 tok] = Q[:, cols_c] . K[:, cols_c]^T  (M=128, N=64)
 //   PV   : O_c[128 rows x 256]   += P[128 x 64] . V[64 x cols_c(256)] (M=128, N=256)
 // where each CTA's 256 V columns are exactly the first four 64-column chunks it
@@ -28,8 +26,8 @@
 //   warp 0     TMA producer: Q once, then per page a block-table lookup and the
 //              CTA's columns of the page into a 4-stage ring (bf16: one 3-D box
 //              of four 64x64 chunks, 128B swizzle, and one 32-column k_pe box,
-//              64B swizzle; FP8: 4 or 5 boxes of 64x64 bytes); owns the TMEM
-//              allocation.
+//              64B swizzle; FP8: four boxes of 64x64 e4m3 bytes and one of
+//              32x64); owns the TMEM allocation.
 //   warp 1     QK^T issuer (one thread).
 //   warps 2-5  softmax / exchange / epilogue warpgroup.  Warp w reads TMEM lane
 //              quadrant w%4 (rows 32*(w%4) .. +31) and works on its CTA's token
@@ -62,10 +60,9 @@ namespace {
 using namespace ptx;
 
 constexpr int kRows = 128;              // query rows per cluster
-constexpr int kMaxCh = 5;               // FP8 cache: 64-column chunks a CTA holds (CTA 0: 4, CTA 1: 5)
 constexpr int kQChunkBytes = 128 * 128;  // 128 rows x 128 B
 constexpr int kKvChunkBytes = 64 * 128;  // 64 tokens x 128 B
-constexpr int kPeHalfBytes = 64 * 64;    // 64 tokens x 32 k_pe columns (bf16 cache: 64-byte rows)
+constexpr int kPeHalfBytes = 64 * 64;    // 64 tokens x 32 k_pe columns in bf16 (64-byte rows)
 constexpr int kMaxStages = 5;  // page stages in the ring (at most)
 constexpr int kSinQuadBytes = 32 * 32 * 4;    // peer's partial S: 32 rows x 32 tokens of one quadrant
 constexpr int kSinBytes = 4 * kSinQuadBytes;
@@ -73,26 +70,29 @@ constexpr int kPBytes = kRows * 128;    // P[128 rows x 64 tokens] bf16
 constexpr int kPHalfBytes = kPBytes / 2;  // one token half of P
 constexpr int kStageOff = 0;
 constexpr int kCtlBytes = 2048;
+constexpr int kRawBox = 64 * 64;          // FP8: one 64 tokens x 64 bytes box of e4m3 c_kv
+constexpr int kRawPeBox = 64 * 32;        // FP8: 64 tokens x 32 bytes of e4m3 k_pe
 
-// Shared-memory layout.  bf16 cache: each CTA holds four c_kv chunks and half of
-// k_pe (32 columns, 64-byte swizzled rows) of every page, so QK^T is 18 MMAs in
-// both CTAs.  FP8 cache: CTA 1 holds the whole k_pe chunk (the converter works
-// in 64-column chunks), 16 and 20 MMAs.
+// Shared-memory layout.  Each CTA holds four c_kv chunks and half of k_pe (32
+// columns, 64-byte swizzled rows) of every page in bf16, so QK^T is 18 MMAs in
+// both CTAs.  With an FP8 cache the e4m3 bytes land in the upper half of the
+// stage and the converter writes the bf16 tiles over the whole stage.
 template <bool kFp8>
 struct Layout {
-  static constexpr int kStageBytes = kFp8 ? kMaxCh * kKvChunkBytes : 4 * kKvChunkBytes + kPeHalfBytes;
+  static constexpr int kStageBytes = 4 * kKvChunkBytes + kPeHalfBytes;
   static constexpr int kStages = 4;                                  // page stages in the ring
   // Q's c_kv chunks land in the last two stages' space, then go to TMEM.
   static constexpr int kQStageOff = kStageOff + (kStages - 2) * kStageBytes;
   static constexpr int kSinOff = kStageOff + kStages * kStageBytes;  // S_in: the peer's partial scores, per quadrant
   static constexpr int kSoutOff = kSinOff + kSinBytes;               // S_out: partial scores staged for the peer
-  static constexpr int kPBufs = kFp8 ? 1 : 2;                        // P buffers (FP8: no room for two)
+  static constexpr int kPBufs = 2;                                   // P buffers
   static constexpr int kPOff = kSoutOff + kSinBytes;
   static constexpr int kQpeOff = kPOff + kPBufs * kPBytes;           // q_pe columns (A from shared memory)
-  static constexpr int kQpeBytes = kFp8 ? kQChunkBytes : kQChunkBytes / 2;
+  static constexpr int kQpeBytes = kQChunkBytes / 2;
   static constexpr int kCtlOff = kQpeOff + kQpeBytes;
   static constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;    // + alignment slack
   static constexpr int kRawOff = kStageBytes / 2;                    // FP8: e4m3 columns in the upper half of a stage
+  static constexpr int kRawPeOff = kRawOff + 4 * kRawBox;            // FP8: the 32 e4m3 k_pe columns
   static_assert(4 * kQChunkBytes <= 2 * kStageBytes, "Q staging");
   static_assert(kStages >= 3 && kStages <= kMaxStages, "stages");
   static_assert(kSmemBytes <= 232448, "shared memory");
@@ -105,13 +105,13 @@ constexpr uint32_t kColS = 256;  // S: two 64-column buffers
 constexpr uint32_t kColQ = 384;  // Q's c_kv chunks as the A operand: 2 bf16 per column, 128 columns
 
 constexpr int kSoftmaxWarp0 = 2;
+constexpr int kLptMaxBatch = 1024;  // requests ranked by length in each CTA up to this batch
 constexpr int kConvWarp0 = 6;    // FP8 converter warps 6-9
 constexpr int kSendWarp0 = 6;    // bf16 cache: S sender warps 6-9
 template <bool kFp8>
 __host__ __device__ constexpr int pv_warp() { return 10; }
 template <bool kFp8>
 __host__ __device__ constexpr int block_threads() { return 32 * (pv_warp<kFp8>() + 1); }
-constexpr int kRawBox = 64 * 64;          // one 64 tokens x 64 bytes box
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -144,6 +144,7 @@ struct Ctl {
   uint64_t fin;                // the peer's row sums delivered (count 4 + 512 B)
   uint64_t drain;
   uint32_t tmem_base;
+  int req;                     // the request this cluster works on
   int abort;
   int poisoned;
   float u_peer[2][kRows];      // [P buffer][row]: reference the peer computed its half with
@@ -211,7 +212,7 @@ __device__ __forceinline__ bool wait_bar(Ctl* c, uint64_t* bar, uint32_t parity,
     if (*(volatile int*)&c->abort) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *(volatile int*)&c->abort = 1;
-      report_error(p.err, MLA_ERR_TIMEOUT, blockIdx.z, where, blockIdx.y);
+      report_error(p.err, MLA_ERR_TIMEOUT, c->req, where, blockIdx.y);
       return false;
     }
   }
@@ -240,22 +241,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   const int lane = threadIdx.x & 31;
   const uint32_t cta = cluster_ctarank();  // 0 or 1: which column half this CTA holds
   const uint32_t peer = cta ^ 1u;
-  const int nch = cta == 0 ? 4 : 5;        // 64-column chunks held
   const int g0 = cta == 0 ? 0 : 4;         // first global chunk
   const int rg = blockIdx.x >> 1;          // row group
   const int split = blockIdx.y;
-  const int b = blockIdx.z;
 
-  const int L = p.seq_lens[b];
-  const bool len_ok = seq_len_ok(p, L);
-  const int lo = split * p.chunk_tokens;
-  const int hi = len_ok ? min(lo + p.chunk_tokens, L) : lo;
-  const int first_page = lo / kPage;
-  const int n_pages = hi > lo ? (hi + kPage - 1) / kPage - first_page : 0;
-  const int row0 = rg * kRows;
-  const float kv_scale = (kFp8 && p.kv_scale) ? *p.kv_scale : 1.0f;
-  const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride + first_page;
-
+  // The barriers and the TMEM allocation do not depend on the request: set them
+  // up while the lengths are fetched.
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
     for (int s = 0; s < kNS; ++s) {
@@ -282,13 +273,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     mbar_init(&ctl->fin, 4);
     mbar_init(&ctl->drain, 2);  // both MMA-issuing threads' last commits
     ctl->abort = 0;
-    ctl->poisoned = len_ok ? 0 : 1;
     fence_mbarrier_init();
-    if (!len_ok && split == 0 && rg == 0 && cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, -1, L);
   }
+
   if (warp == 0) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
+  }
+
+  // Clusters take the requests in order of decreasing length (ties by index):
+  // the hardware starts clusters in grid order, so the longest requests start
+  // first and the short ones fill the last waves (longest processing time
+  // first).  The lengths are ranked in shared memory (the P buffer, idle until
+  // the page loop); larger batches keep the index order.
+  const bool lpt = p.batch <= kLptMaxBatch;
+  int* lens = reinterpret_cast<int*>(sP);
+  const int nb4 = (p.batch + 3) >> 2;  // padded with INT_MIN, which never outranks anything
+  if (lpt)
+    for (int i = threadIdx.x; i < 4 * nb4; i += blockDim.x) lens[i] = i < p.batch ? p.seq_lens[i] : INT_MIN;
+  __syncthreads();
+  if (lpt) {
+    for (int c = threadIdx.x; c < p.batch; c += blockDim.x) {
+      const int lc = lens[c];
+      int rank = 0;
+#pragma unroll 4
+      for (int k4 = 0; k4 < nb4; ++k4) {
+        const int4 l4 = reinterpret_cast<const int4*>(lens)[k4];
+        const int k = 4 * k4;
+        rank += (l4.x > lc) | ((l4.x == lc) & (k < c));
+        rank += (l4.y > lc) | ((l4.y == lc) & (k + 1 < c));
+        rank += (l4.z > lc) | ((l4.z == lc) & (k + 2 < c));
+        rank += (l4.w > lc) | ((l4.w == lc) & (k + 3 < c));
+      }
+      if (rank == (int)blockIdx.z) ctl->req = c;
+    }
+  } else if (threadIdx.x == 0) {
+    ctl->req = blockIdx.z;
+  }
+  __syncthreads();
+  const int b = ctl->req;
+
+  const int L = lpt ? lens[b] : p.seq_lens[b];
+  const bool len_ok = seq_len_ok(p, L);
+  const int lo = split * p.chunk_tokens;
+  const int hi = len_ok ? min(lo + p.chunk_tokens, L) : lo;
+  const int first_page = lo / kPage;
+  const int n_pages = hi > lo ? (hi + kPage - 1) / kPage - first_page : 0;
+  const int row0 = rg * kRows;
+  const float kv_scale = (kFp8 && p.kv_scale) ? *p.kv_scale : 1.0f;
+  const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride + first_page;
+
+  // Thread 0 is the TMA producer: it starts Q's loads (into this CTA's own
+  // shared memory, on a barrier it initialised itself) and the first
+  // block-table lookup before the cluster-wide sync.
+  int page_first = 0;
+  if (threadIdx.x == 0) {
+    ctl->poisoned = len_ok ? 0 : 1;
+    if (!len_ok && split == 0 && rg == 0 && cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, -1, L);
+    if (n_pages > 0) {
+      page_first = bt_row[0];
+      fence_proxy_async_smem();  // the barrier initialisations are visible to the copy engine
+      prefetch_tmap(&tm_qn);
+      prefetch_tmap(&tm_qp);
+      const int qrow = b * p.rows + row0;
+      mbar_arrive_expect_tx(&ctl->q_full, 4 * kQChunkBytes + kQChunkBytes / 2);
+      for (int k = 0; k < 4; ++k) tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, (g0 + k) * 64, qrow);
+      tma_load_2d(sQpe, &tm_qp, &ctl->q_full, 32 * (int)cta, qrow);
+      prefetch_tmap(&tm_kv);
+      if (!kFp8) prefetch_tmap(&tm_kv3);
+      prefetch_tmap(&tm_kpe);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -298,29 +352,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_pages > 0) {
-      prefetch_tmap(&tm_kv);
-      if (!kFp8) {
-        prefetch_tmap(&tm_kv3);
-        prefetch_tmap(&tm_kpe);
-      }
-      const int qrow = b * p.rows + row0;
-      if (kFp8) {
-        mbar_arrive_expect_tx(&ctl->q_full, nch * kQChunkBytes);
-        for (int k = 0; k < nch; ++k) {
-          const int g = g0 + k;
-          if (g < 8)
-            tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, g * 64, qrow);
-          else
-            tma_load_2d(sQpe, &tm_qp, &ctl->q_full, 0, qrow);
-        }
-      } else {  // four c_kv chunks and this CTA's 32 q_pe columns
-        mbar_arrive_expect_tx(&ctl->q_full, 4 * kQChunkBytes + kQChunkBytes / 2);
-        for (int k = 0; k < 4; ++k) tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, (g0 + k) * 64, qrow);
-        tma_load_2d(sQpe, &tm_qp, &ctl->q_full, 32 * (int)cta, qrow);
-      }
+    if (lane == 0 && n_pages > 0) {  // Q is on its way (see above)
       int issued = 0;
-      int next_page = bt_row[0];
+      int next_page = page_first;
       for (int j = 0; j < n_pages; ++j) {
         const int s = j % kNS;
         const int page = next_page;
@@ -333,10 +367,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         if (page < 0 || page >= p.num_pages) {
           if (cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, first_page + j, page);
           mbar_arrive(land);  // nothing to load; consumers mask the whole page
-        } else if (kFp8) {
-          mbar_arrive_expect_tx(land, nch * kRawBox);
-          for (int k = 0; k < nch; ++k)
+        } else if (kFp8) {  // e4m3: the CTA's four c_kv chunks and 32 k_pe columns
+          mbar_arrive_expect_tx(land, 4 * kRawBox + kRawPeBox);
+          for (int k = 0; k < 4; ++k)
             tma_load_2d(stage + Lay::kRawOff + k * kRawBox, &tm_kv, land, (g0 + k) * 64, page * kPage);
+          tma_load_2d(stage + Lay::kRawPeOff, &tm_kpe, land, 8 * 64 + 32 * (int)cta, page * kPage);
         } else {
           // The CTA's four c_kv chunks in one 3-D box (columns x rows x chunks),
           // which lands as [chunk][row][128 B], and its 32 k_pe columns in a 2-D
@@ -363,7 +398,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // runs ahead.
     if (lane == 0 && n_pages > 0) {
       const uint32_t kv_addr = smem_u32(sKV);
-      const uint64_t qpe_desc = kFp8 ? sdesc_sw128(smem_u32(sQpe), 16, 1024) : sdesc_sw64(smem_u32(sQpe), 16, 512);
+      const uint64_t qpe_desc = sdesc_sw64(smem_u32(sQpe), 16, 512);
       bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
       for (int j = 0; ok && j < n_pages; ++j) {
         if (!wait_bar(ctl, &ctl->full[j % kNS], (j / kNS) & 1, p, 3) ||
@@ -378,14 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
             mma_bf16_ts(d, tmem + kColQ + k * 32 + kk * 8, k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4),
                         kIdescQK, (k | kk) ? 1u : 0u);
         }
-        if (kFp8) {
-          if (nch == 5) {  // k_pe: A = q_pe from shared memory
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4),
-                          k_desc + (uint64_t)((4 * kKvChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
-          }
-        } else {  // this CTA's 32 k_pe columns: two K-steps along 64-byte swizzled rows
+        {  // this CTA's 32 k_pe columns: two K-steps along 64-byte swizzled rows
           const uint64_t kpe_desc = sdesc_sw64(kv_addr + (j % kNS) * kStageBytes + 4 * kKvChunkBytes, 16, 512);
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
@@ -442,41 +470,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     }
   } else if (kFp8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
     // ------------------------------------------------------------ e4m3 -> bf16 converter
+    // Thread ct converts tokens ct/2 of chunks 2(ct%2) and 2(ct%2)+1 (64 e4m3
+    // bytes each, into 128-byte swizzled bf16 rows), and threads below 64 also
+    // token ct's 32 k_pe bytes (into 64-byte swizzled rows).
     const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
-    const int units = nch * 64;                    // (chunk, token) pairs of 64 bytes
+    const int t_c = ct >> 1, c0 = 2 * (ct & 1);
     for (int j = 0; j < n_pages; ++j) {
       const int s = j % kNS;
       if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[s], (j / kNS) & 1, p, 9))) break;
       uint8_t* stage = sKV + s * kStageBytes;
-      uint4 raw[3][4];
+      uint4 raw[2][4], rpe[2];
 #pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        const int u = ct + k * 128;
-        if (u < units) {
-          const uint4* src = reinterpret_cast<const uint4*>(stage + Lay::kRawOff + (u >> 6) * kRawBox + (u & 63) * 64);
+      for (int k = 0; k < 2; ++k) {
+        const uint4* src = reinterpret_cast<const uint4*>(stage + Lay::kRawOff + (c0 + k) * kRawBox + t_c * 64);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) raw[k][q] = src[q];
-        }
+        for (int q = 0; q < 4; ++q) raw[k][q] = src[q];
+      }
+      if (ct < 64) {
+        const uint4* src = reinterpret_cast<const uint4*>(stage + Lay::kRawPeOff + ct * 32);
+        rpe[0] = src[0];
+        rpe[1] = src[1];
       }
       conv_sync();  // every raw byte is in registers before the bf16 writes overlap them
 #pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        const int u = ct + k * 128;
-        if (u < units) {
-          const int c = u >> 6, t = u & 63;
-          uint8_t* dst = stage + c * kKvChunkBytes + t * 128;
+      for (int k = 0; k < 2; ++k) {
+        uint8_t* dst = stage + (c0 + k) * kKvChunkBytes + t_c * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t w[4] = {raw[k][q].x, raw[k][q].y, raw[k][q].z, raw[k][q].w};
-            uint32_t o[8];
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t w[4] = {raw[k][q].x, raw[k][q].y, raw[k][q].z, raw[k][q].w};
+          uint32_t o[8];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              o[2 * h] = e4m3x2_to_bf16x2((uint16_t)(w[h] & 0xFFFFu));
-              o[2 * h + 1] = e4m3x2_to_bf16x2((uint16_t)(w[h] >> 16));
-            }
-            *reinterpret_cast<uint4*>(dst + (((2 * q) ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          for (int h = 0; h < 4; ++h) {
+            o[2 * h] = e4m3x2_to_bf16x2((uint16_t)(w[h] & 0xFFFFu));
+            o[2 * h + 1] = e4m3x2_to_bf16x2((uint16_t)(w[h] >> 16));
           }
+          *reinterpret_cast<uint4*>(dst + (((2 * q) ^ (t_c & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ (t_c & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+      }
+      if (ct < 64) {
+        uint8_t* dst = stage + 4 * kKvChunkBytes + ct * 64;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t w[4] = {rpe[q].x, rpe[q].y, rpe[q].z, rpe[q].w};
+          uint32_t o[8];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            o[2 * h] = e4m3x2_to_bf16x2((uint16_t)(w[h] & 0xFFFFu));
+            o[2 * h + 1] = e4m3x2_to_bf16x2((uint16_t)(w[h] >> 16));
+          }
+          *reinterpret_cast<uint4*>(dst + (((2 * q) ^ ((ct >> 1) & 3)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ ((ct >> 1) & 3)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
       }
       fence_proxy_async_smem();
@@ -1013,10 +1057,8 @@ cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
   const uint64_t kv_rows = (uint64_t)p.num_pages * kPage;
   if (!encode_2d(&tm_qn, p.q_nope, kKvLora, q_rows, p.q_nope_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !(p.kv_fp8 ? encode_2d(&tm_qp, p.q_pe, kRope, q_rows, p.q_pe_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                             128, CU_TENSOR_MAP_SWIZZLE_128B)
-                 : encode_2d(&tm_qp, p.q_pe, kRope, q_rows, p.q_pe_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                             128, CU_TENSOR_MAP_SWIZZLE_64B, 32)))
+      !encode_2d(&tm_qp, p.q_pe, kRope, q_rows, p.q_pe_stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128,
+                 CU_TENSOR_MAP_SWIZZLE_64B, 32))
     return cudaErrorInvalidValue;
   const bool ok = p.kv_fp8 ? encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64,
                                        CU_TENSOR_MAP_SWIZZLE_NONE)
@@ -1025,11 +1067,13 @@ cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
   if (!ok) return cudaErrorInvalidValue;
   // bf16 cache viewed as [chunk 0..8][row][64 columns]: row stride 1152 B, chunk stride 128 B.
   if (!p.kv_fp8 && !encode_kv_chunks(&tm_kv3, p.kv, kv_rows)) return cudaErrorInvalidValue;
-  // bf16 cache: 32 k_pe columns per box, 64-byte swizzled rows.
-  if (!p.kv_fp8 && !encode_2d(&tm_kpe, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
-                              CU_TENSOR_MAP_SWIZZLE_64B, 32))
+  // 32 k_pe columns per box: bf16 with 64-byte swizzled rows, or 32 e4m3 bytes.
+  if (!(p.kv_fp8 ? encode_2d(&tm_kpe, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64,
+                             CU_TENSOR_MAP_SWIZZLE_NONE, 32)
+                 : encode_2d(&tm_kpe, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
+                             CU_TENSOR_MAP_SWIZZLE_64B, 32)))
     return cudaErrorInvalidValue;
-  if (p.kv_fp8) tm_kv3 = tm_kpe = tm_kv;  // unused on the FP8 path
+  if (p.kv_fp8) tm_kv3 = tm_kv;  // unused on the FP8 path
   const dim3 grid(2 * p.row_groups, p.splits, p.batch);
   if (p.kv_fp8) {
     auto kern = split_kv_tc_kernel<true>;
