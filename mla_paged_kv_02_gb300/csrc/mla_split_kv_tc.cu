@@ -245,8 +245,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   const int rg = blockIdx.x >> 1;          // row group
   const int split = blockIdx.y;
 
-  // The barriers and the TMEM allocation do not depend on the request: set them
-  // up while the lengths are fetched.
+  // The lengths are fetched first (each thread one, more for big batches) so
+  // that their latency overlaps the barrier set-up and the TMEM allocation,
+  // which do not depend on the request.
+  const bool lpt = p.batch <= kLptMaxBatch;
+  const int nb4 = (p.batch + 3) >> 2;  // lengths padded with INT_MIN, which never outranks anything
+  const int my_len = (lpt && (int)threadIdx.x < p.batch) ? p.seq_lens[threadIdx.x] : INT_MIN;
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
     for (int s = 0; s < kNS; ++s) {
@@ -286,11 +290,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   // first and the short ones fill the last waves (longest processing time
   // first).  The lengths are ranked in shared memory (the P buffer, idle until
   // the page loop); larger batches keep the index order.
-  const bool lpt = p.batch <= kLptMaxBatch;
   int* lens = reinterpret_cast<int*>(sP);
-  const int nb4 = (p.batch + 3) >> 2;  // padded with INT_MIN, which never outranks anything
-  if (lpt)
-    for (int i = threadIdx.x; i < 4 * nb4; i += blockDim.x) lens[i] = i < p.batch ? p.seq_lens[i] : INT_MIN;
+  if (lpt) {
+    if ((int)threadIdx.x < 4 * nb4) lens[threadIdx.x] = my_len;
+    for (int i = threadIdx.x + blockDim.x; i < 4 * nb4; i += blockDim.x) lens[i] = i < p.batch ? p.seq_lens[i] : INT_MIN;
+  }
   __syncthreads();
   if (lpt) {
     for (int c = threadIdx.x; c < p.batch; c += blockDim.x) {

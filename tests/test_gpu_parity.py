@@ -150,6 +150,33 @@ def test_page_permutation_bitwise():
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_request_order_does_not_matter():
+    # Clusters take the requests in order of decreasing length; reordering the
+    # batch (ties included) must reorder the results and change nothing else.
+    lens = [700, 64, 2, 700, 2000, 65, 64, 1300]
+    inp = small(650, 2, lens, H=32, sharp=3.0)
+    perm = torch.tensor([5, 2, 7, 0, 3, 6, 1, 4])
+    sub = synth.Inputs(**{**inp.__dict__})
+    sub.q_nope = inp.q_nope[perm].contiguous()
+    sub.q_pe = inp.q_pe[perm].contiguous()
+    sub.block_table = inp.block_table[perm].contiguous()
+    sub.seq_lens = inp.seq_lens[perm].contiguous()
+    for s in (0, 1, 3):
+        o1, l1, _ = run(inp, force_splits=s)
+        o2, l2, _ = run(sub, force_splits=s)
+        assert torch.equal(o1[perm], o2) and torch.equal(l1[perm], l2)
+
+
+def test_batch_above_ranking_limit():
+    # Batches above the in-kernel ranking limit keep the index order.
+    g = np.random.default_rng(11)
+    lens = [int(x) for x in g.integers(1, 130, size=1100)]
+    inp = small(660, 1, lens, H=16)
+    ref_o, ref_l = oracle.decode(inp)
+    out, lse, _ = run(inp, out_fp32=True)
+    compare(out, lse, ref_o, ref_l, what="B=1100")
+
+
 def test_split_count_independence():
     inp = small(700, 4, [4, 500, 2000, 4096], H=32, sharp=5.0)
     ref_o, ref_l = oracle.decode(inp)
