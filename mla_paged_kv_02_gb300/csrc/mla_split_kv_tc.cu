@@ -22,7 +22,7 @@
 // maxima and row sums go by st.async.  Both complete transaction bytes on the
 // receiver's mbarrier.
 //
-// Warp roles (352 threads):
+// Warp roles (352 threads; 480 with an FP8 cache):
 //   warp 0     TMA producer: Q once, then per page a block-table lookup and the
 //              CTA's columns of the page into a 4-stage ring (bf16: one 3-D box
 //              of four 64x64 chunks, 128B swizzle, and one 32-column k_pe box,
@@ -34,14 +34,15 @@
 //              half of those rows.  Online softmax in the exp2 domain with lazily
 //              raised whole-number reference maxima, agreed between the pair one
 //              page behind (see the warpgroup's comment).
-//   warps 6-9  (bf16 cache) S senders: the peer's token half of S(j) from TMEM
-//              to the peer, off the softmax warps' chain.
+//   warps 6-9  (bf16 cache; 10-13 with an FP8 cache) S senders: the peer's
+//              token half of S(j) from TMEM to the peer, off the softmax warps'
+//              chain.
 //   warps 6-9  (FP8 cache) converter: the CTA's e4m3 columns land in the upper
 //              half of a stage; every thread first pulls its share into
 //              registers, then writes exact bf16 values (e4m3 is a subset of
 //              bf16) in the swizzled layout.  The per-tensor scale is folded into
 //              the softmax scale and the epilogue.
-//   warp 10    PV issuer (one thread).
+//   warp 10    PV issuer (one thread; warp 14 with an FP8 cache).
 //
 // Q's c_kv columns are kept in tensor memory as the A operand of QK^T (read every
 // page; from TMEM they cost no shared-memory bandwidth and leave room for 4 page
@@ -107,9 +108,10 @@ constexpr uint32_t kColQ = 384;  // Q's c_kv chunks as the A operand: 2 bf16 per
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kLptMaxBatch = 1024;  // requests ranked by length in each CTA up to this batch
 constexpr int kConvWarp0 = 6;    // FP8 converter warps 6-9
-constexpr int kSendWarp0 = 6;    // bf16 cache: S sender warps 6-9
 template <bool kFp8>
-__host__ __device__ constexpr int pv_warp() { return 10; }
+__host__ __device__ constexpr int send_warp0() { return kFp8 ? 10 : 6; }  // S sender warps
+template <bool kFp8>
+__host__ __device__ constexpr int pv_warp() { return kFp8 ? 14 : 10; }
 template <bool kFp8>
 __host__ __device__ constexpr int block_threads() { return 32 * (pv_warp<kFp8>() + 1); }
 
@@ -261,8 +263,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     mbar_init(&ctl->q_tmem, 4);
     mbar_init(&ctl->s_full[0], 1);
     mbar_init(&ctl->s_full[1], 1);
-    mbar_init(&ctl->s_free[0], kFp8 ? 4 : 8);  // softmax warps (+ sender warps)
-    mbar_init(&ctl->s_free[1], kFp8 ? 4 : 8);
+    mbar_init(&ctl->s_free[0], 8);  // softmax and sender warps
+    mbar_init(&ctl->s_free[1], 8);
     for (int q = 0; q < 4; ++q) {
       mbar_init(&ctl->sin_full[q], 1);
       mbar_init(&ctl->sin_free[q], 1);
@@ -531,8 +533,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       conv_sync();
       if (lane == 0) mbar_arrive(&ctl->full[s]);
     }
-  } else if (!kFp8 && warp >= kSendWarp0 && warp < kSendWarp0 + 4) {
-    // ------------------------------------------------------------ S sender (bf16 cache)
+  } else if (warp >= send_warp0<kFp8>() && warp < send_warp0<kFp8>() + 4) {
+    // ------------------------------------------------------------ S sender
     // The peer's token half of S(j), for the rows of TMEM lane quadrant w%4, goes
     // from TMEM through S_out to the peer's S_in as one 4 KB bulk copy, as soon as
     // QK(j) is done and the peer has consumed the previous page's partial (which
@@ -596,12 +598,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     const float sc2 = p.softmax_scale * kv_scale * kLog2e;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t col_own = kColS + 32 * cta;    // S columns of this CTA's token half (within a buffer)
-    const uint32_t col_oth = kColS + 32 * peer;
     uint8_t* sin_row = sSin + quad * kSinQuadBytes + lane * 128;  // 32 fp32 of the peer's partial
-    uint8_t* sout_quad = sSout + quad * kSinQuadBytes;
-    uint8_t* sout_row = sout_quad + lane * 128;
-    const uint32_t sin_quad_peer = mapa_shared(smem_u32(sSin + quad * kSinQuadBytes), peer);
-    const uint32_t sin_full_peer = mapa_shared(smem_u32(&ctl->sin_full[quad]), peer);
     const uint32_t sin_free_peer = mapa_shared(smem_u32(&ctl->sin_free[quad]), peer);
     const uint32_t p_peer = mapa_shared(smem_u32(sP), peer);
     float r_ref = -INFINITY;   // reference this CTA computes P with
@@ -618,39 +615,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     };
     const int p_mine_off = (int)cta * kPHalfBytes + quad * 2048;  // this warp's rows of this CTA's half
 
-    // S(jj) from TMEM: this CTA's token half goes to `own`.  The peer's half goes
-    // to the peer's S_in for this quadrant as one 4 KB bulk copy, staged in S_out:
-    // with a bf16 cache the sender warps do that, with an FP8 cache (no room for
-    // more warps) this warp does, once the peer has consumed the previous page's
-    // (which also means the previous copy has read S_out).  The copy engine
-    // carries the bytes, so no warp stalls on the pair's link.
+    // This CTA's token half of S(jj) from TMEM into `own` (the sender warps
+    // take the peer's half).
     auto take_s = [&](int jj, float (&own)[32]) -> bool {
       const int sb = jj & 1;
       if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[sb], (jj >> 1) & 1, p, 6))) return false;
       tc_fence_after();
-      uint32_t mine[2][16], oth[2][16];
+      uint32_t mine[2][16];
       tmem_ld16(tmem + lane_base + col_own + sb * 64, mine[0]);
       tmem_ld16(tmem + lane_base + col_own + sb * 64 + 16, mine[1]);
-      if (kFp8) {
-        tmem_ld16(tmem + lane_base + col_oth + sb * 64, oth[0]);
-        tmem_ld16(tmem + lane_base + col_oth + sb * 64 + 16, oth[1]);
-      }
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
 #pragma unroll
       for (int k = 0; k < 32; ++k) own[k] = __uint_as_float(mine[k >> 4][k & 15]);
-      if (!kFp8) return true;
-      if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->sin_free[quad], (jj & 1) ^ 1, p, 13))) return false;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(sout_row + ((u ^ (lane & 7)) << 4)) =
-            make_uint4(oth[u >> 2][(u & 3) * 4], oth[u >> 2][(u & 3) * 4 + 1], oth[u >> 2][(u & 3) * 4 + 2],
-                       oth[u >> 2][(u & 3) * 4 + 3]);
-      fence_proxy_async_smem();  // staged rows visible to the copy engine
-      __syncwarp();
-      if (lane == 0) bulk_copy_to_peer(sin_quad_peer, sout_quad, kSinQuadBytes, sin_full_peer);
       return true;
     };
 
