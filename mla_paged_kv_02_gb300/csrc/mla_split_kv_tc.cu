@@ -575,9 +575,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // page a warp hands the peer the partial scores of the peer's token half,
     // adds the peer's partial for its own half, and computes P for its half, which
     // it writes into both CTAs' P buffers.  Order within page j: add the peer's
-    // partial of S(j); settle and send the reference; P(j) out; S(j+1) out; check
-    // page j.  P(j) leaves before S(j+1) is taken so that PV(j), and with it the
-    // release of page j's stage for the next load, is not held up by the exchange.
+    // partial of S(j); settle and send the reference; P(j) out; check page j;
+    // own half of S(j+1) from TMEM.  P(j) and the check come first so that PV(j),
+    // and with it the release of page j's stage for the next load, is not held
+    // up by the next page.
     //
     // Reference maxima.  P of one row must share one reference across both
     // halves, yet neither CTA sees the other's scores.  Each CTA computes with
@@ -872,13 +873,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         const int off = pb * kPBytes + p_mine_off;
         bulk_copy_to_peer(p_peer + (uint32_t)off, sP + off, 2048, pv_bar_peer);
       }
-      // Then the next page's scores to the peer, and this page's reference
-      // check, after which PV(j) may go as soon as the peer's P is in.
-      if (j + 1 < n_pages && !take_s(j + 1, sv_next)) {
+      // Then this page's reference check, after which PV(j) may go (the own
+      // half at once, the peer's half when its P is in), and the own half of the
+      // next page's scores.
+      if (!check(j, u_cur)) {
         ok = false;
         break;
       }
-      if (!check(j, u_cur)) {
+      if (j + 1 < n_pages && !take_s(j + 1, sv_next)) {
         ok = false;
         break;
       }
