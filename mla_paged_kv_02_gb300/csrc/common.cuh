@@ -40,7 +40,11 @@ struct DecodeParams {
   int32_t* err;     // workspace header
   int batch, num_heads, q_len, rows;  // rows = num_heads * q_len per request
   int max_seq_len, splits, chunk_tokens, rows_per_cta, row_groups;
+  int order_by_length;  // clusters take the requests longest first (see kMaxOrderedBatch)
 };
+
+// Batches up to this size are ranked by length inside the split kernel.
+constexpr int kMaxOrderedBatch = 1024;
 
 // Records the first device-side error of a call sequence (sticky until read).
 __device__ __forceinline__ void report_error(int32_t* err, int code, int request, int index,

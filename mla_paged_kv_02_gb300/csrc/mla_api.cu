@@ -79,6 +79,10 @@ mla_status_t fill_params(const mla_decode_plan_t* pl, const void* q_nope, int64_
   p->chunk_tokens = pl->chunk_tokens;
   p->rows_per_cta = pl->rows_per_cta;
   p->row_groups = pl->row_groups;
+  // Longest requests first, when more clusters than the GPU holds at once wait
+  // to start (with a single wave the order does not matter).
+  const int64_t clusters = (int64_t)pl->batch * pl->row_groups * pl->num_kv_splits;
+  p->order_by_length = pl->batch <= kMaxOrderedBatch && clusters > pl->num_sms / 2;
   return MLA_OK;
 }
 

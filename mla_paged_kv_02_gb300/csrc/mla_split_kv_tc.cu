@@ -106,7 +106,6 @@ constexpr uint32_t kColS = 256;  // S: two 64-column buffers
 constexpr uint32_t kColQ = 384;  // Q's c_kv chunks as the A operand: 2 bf16 per column, 128 columns
 
 constexpr int kSoftmaxWarp0 = 2;
-constexpr int kLptMaxBatch = 1024;  // requests ranked by length in each CTA up to this batch
 constexpr int kConvWarp0 = 6;    // FP8 converter warps 6-9
 template <bool kFp8>
 __host__ __device__ constexpr int send_warp0() { return kFp8 ? 10 : 6; }  // S sender warps
@@ -250,7 +249,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   // The lengths are fetched first (each thread one, more for big batches) so
   // that their latency overlaps the barrier set-up and the TMEM allocation,
   // which do not depend on the request.
-  const bool lpt = p.batch <= kLptMaxBatch;
+  const bool lpt = p.order_by_length != 0;
   const int nb4 = (p.batch + 3) >> 2;  // lengths padded with INT_MIN, which never outranks anything
   const int my_len = (lpt && (int)threadIdx.x < p.batch) ? p.seq_lens[threadIdx.x] : INT_MIN;
   if (threadIdx.x == 0) {
@@ -291,7 +290,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   // the hardware starts clusters in grid order, so the longest requests start
   // first and the short ones fill the last waves (longest processing time
   // first).  The lengths are ranked in shared memory (the P buffer, idle until
-  // the page loop); larger batches keep the index order.
+  // the page loop).  The host turns this off for batches above
+  // kMaxOrderedBatch and for grids that start in a single wave.
   int* lens = reinterpret_cast<int*>(sP);
   if (lpt) {
     if ((int)threadIdx.x < 4 * nb4) lens[threadIdx.x] = my_len;

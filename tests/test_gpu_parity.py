@@ -151,11 +151,14 @@ def test_page_permutation_bitwise():
 
 
 def test_request_order_does_not_matter():
-    # Clusters take the requests in order of decreasing length; reordering the
-    # batch (ties included) must reorder the results and change nothing else.
-    lens = [700, 64, 2, 700, 2000, 65, 64, 1300]
-    inp = small(650, 2, lens, H=32, sharp=3.0)
-    perm = torch.tensor([5, 2, 7, 0, 3, 6, 1, 4])
+    # Clusters take the requests in order of decreasing length (when the grid
+    # takes more than one wave); reordering the batch, ties included, must
+    # reorder the results and change nothing else.  40 requests x 2 row groups
+    # start in more than one wave on any GPU with fewer than 160 SMs.
+    g = np.random.default_rng(12)
+    lens = [int(x) for x in g.choice([4, 64, 65, 700, 1300, 2000], size=40)]
+    inp = small(650, 4, lens, H=64, sharp=3.0)
+    perm = torch.from_numpy(g.permutation(40))
     sub = synth.Inputs(**{**inp.__dict__})
     sub.q_nope = inp.q_nope[perm].contiguous()
     sub.q_pe = inp.q_pe[perm].contiguous()
@@ -168,7 +171,7 @@ def test_request_order_does_not_matter():
 
 
 def test_batch_above_ranking_limit():
-    # Batches above the in-kernel ranking limit keep the index order.
+    # Batches above the in-kernel ranking limit (1024) keep the index order.
     g = np.random.default_rng(11)
     lens = [int(x) for x in g.integers(1, 130, size=1100)]
     inp = small(660, 1, lens, H=16)
