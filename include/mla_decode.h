@@ -121,7 +121,8 @@ mla_status_t mla_workspace_init(void* workspace, size_t workspace_bytes, void* c
  * device can see (seq_len out of range, a page index outside [0, num_pages),
  * a wait that timed out) set the sticky error word in the workspace header and
  * the affected request's rows are written as NaN; mla_decode_check_error
- * reports them.  Non-uniform q_len cannot be expressed: there is no fallback.
+ * reports them.  Non-uniform q_len goes through mla_decode_varlen; there is
+ * no fallback.
  */
 mla_status_t mla_decode(const mla_decode_plan_t* plan, const void* q_nope, int64_t q_nope_row_stride,
                         const void* q_pe, int64_t q_pe_row_stride, const void* kv_cache,
@@ -152,6 +153,31 @@ mla_status_t mla_split_kv(const mla_decode_plan_t* plan, const void* q_nope,
 mla_status_t mla_combine(const mla_decode_plan_t* plan, void* out, mla_out_dtype_t out_dtype,
                          float* lse, const void* workspace, size_t workspace_bytes,
                          void* cuda_stream);
+
+/*
+ * mla_decode_varlen -- mla_decode with a number of query tokens per request
+ * (the per-request metadata the TokenSpeed MLA summary asks for in place of a
+ * fallback that unsqueezes non-uniform q_len; vLLM PR #41778, review
+ * highlights and risk 6).
+ *
+ * Same arguments as mla_decode plus
+ *   q_lens : int32 [batch] on the device, 1 <= q_lens[b] <= plan->q_len and
+ *            q_lens[b] <= seq_lens[b]
+ * The layouts stay padded to plan->q_len: request b's query rows are (b, i, h)
+ * for i < q_lens[b]; its query i sees tokens [0, L_b - q_lens[b] + i], so each
+ * request's last query token sits at position L_b - 1.  Rows with
+ * i >= q_lens[b] are padding: their out rows are written as 0 and their lse as
+ * -inf, whatever q_nope/q_pe hold there.  A q_lens[b] out of range is a
+ * device-side input error (index -2, value q_lens[b]) that writes request b's
+ * rows as NaN.  q_lens == NULL returns MLA_ERR_INVALID_ARG.
+ */
+mla_status_t mla_decode_varlen(const mla_decode_plan_t* plan, const void* q_nope,
+                               int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                               const void* kv_cache, int num_pages, const int32_t* block_table,
+                               int block_table_stride, const int32_t* seq_lens, const int32_t* q_lens,
+                               float softmax_scale, const float* kv_scale, void* out,
+                               mla_out_dtype_t out_dtype, float* lse, void* workspace,
+                               size_t workspace_bytes, void* cuda_stream);
 
 /*
  * mla_decode_noalloc -- mla_decode for callers that cannot allocate device

@@ -37,6 +37,7 @@ EXPORTED = (
     "mla_combine",
     "mla_decode_check_error",
     "mla_decode_noalloc",
+    "mla_decode_varlen",
     "mla_status_string",
 )
 
@@ -91,6 +92,7 @@ def load() -> ctypes.CDLL:
     lib.mla_combine.argtypes = [PP, P, I, P, P, SZ, P]
     lib.mla_decode_check_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.mla_decode_noalloc.argtypes = [PP, P, I64, P, I64, P, I, P, I, P, F, P, P, I, P, P]
+    lib.mla_decode_varlen.argtypes = [PP, P, I64, P, I64, P, I, P, I, P, P, F, P, P, I, P, P, SZ, P]
     lib.mla_status_string.argtypes = [I]
     lib.mla_status_string.restype = ctypes.c_char_p
     for name in EXPORTED:
@@ -144,6 +146,14 @@ def decode(pl: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, softmax_scal
     """mla_decode; returns the C status (0 = launched)."""
     return load().mla_decode(*_decode_args(pl, q_nope, q_pe, kv_cache, block_table, seq_lens,
                                            softmax_scale, kv_scale, out, lse, workspace, stream))
+
+
+def decode_varlen(pl: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, q_lens, softmax_scale, kv_scale,
+                  out, lse, workspace, stream=None) -> int:
+    """mla_decode_varlen: per-request q_len (layouts padded to the plan's q_len)."""
+    a = _decode_args(pl, q_nope, q_pe, kv_cache, block_table, seq_lens, softmax_scale, kv_scale, out, lse,
+                     workspace, stream)
+    return load().mla_decode_varlen(*a[:10], _ptr(q_lens), *a[10:])
 
 
 def split_kv(pl: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, softmax_scale, kv_scale, out,

@@ -41,16 +41,25 @@ def kv_scale_tensor(inp) -> Optional[torch.Tensor]:
 
 
 def decode(inp, pl: Optional[_lib.Plan] = None, force_splits: int = 0, out_fp32: Optional[bool] = None,
-           workspace: Optional[torch.Tensor] = None, stream=None, check: bool = True):
-    """Run one decode on ``inp`` (tensors already on the GPU).  Returns (out, lse, plan)."""
+           workspace: Optional[torch.Tensor] = None, stream=None, check: bool = True,
+           q_lens: Optional[torch.Tensor] = None):
+    """Run one decode on ``inp`` (tensors already on the GPU).  Returns (out, lse, plan).
+
+    ``q_lens`` (int32 [B] on the GPU) selects mla_decode_varlen: request b uses
+    its first q_lens[b] query tokens of the padded ``inp.q_len``."""
     if pl is None:
         pl = plan_for(inp, force_splits=force_splits)
     if workspace is None:
         workspace = alloc_workspace(pl, inp.q_nope.device, stream)
     out, lse = alloc_outputs(inp, out_fp32)
     kvs = kv_scale_tensor(inp)
-    st = _lib.decode(pl, inp.q_nope.view(-1, 512), inp.q_pe.view(-1, 64), inp.kv_cache,
-                     inp.block_table, inp.seq_lens, inp.softmax_scale, kvs, out, lse, workspace, stream)
+    if q_lens is None:
+        st = _lib.decode(pl, inp.q_nope.view(-1, 512), inp.q_pe.view(-1, 64), inp.kv_cache,
+                         inp.block_table, inp.seq_lens, inp.softmax_scale, kvs, out, lse, workspace, stream)
+    else:
+        st = _lib.decode_varlen(pl, inp.q_nope.view(-1, 512), inp.q_pe.view(-1, 64), inp.kv_cache,
+                                inp.block_table, inp.seq_lens, q_lens, inp.softmax_scale, kvs, out, lse,
+                                workspace, stream)
     if st != _lib.MLA_OK:
         raise _lib.MlaError(st, "mla_decode")
     if check:

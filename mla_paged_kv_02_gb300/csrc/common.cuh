@@ -31,6 +31,7 @@ struct DecodeParams {
   const int32_t* block_table;
   int bt_stride;
   const int32_t* seq_lens;
+  const int32_t* q_lens;  // [B] per-request number of query tokens (1..q_len), or nullptr: all q_len
   float softmax_scale;
   const float* kv_scale;  // device scalar or nullptr
   void* out;              // [B*R, 512] bf16 or fp32

@@ -219,6 +219,23 @@ mla_status_t mla_decode(const mla_decode_plan_t* plan, const void* q_nope, int64
   return mla_combine(plan, out, out_dtype, lse, workspace, workspace_bytes, cuda_stream);
 }
 
+mla_status_t mla_decode_varlen(const mla_decode_plan_t* plan, const void* q_nope, int64_t q_nope_row_stride,
+                               const void* q_pe, int64_t q_pe_row_stride, const void* kv_cache,
+                               int num_pages, const int32_t* block_table, int block_table_stride,
+                               const int32_t* seq_lens, const int32_t* q_lens, float softmax_scale,
+                               const float* kv_scale, void* out, mla_out_dtype_t out_dtype, float* lse,
+                               void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (!q_lens) return MLA_ERR_INVALID_ARG;
+  DecodeParams p;
+  mla_status_t st = fill_params(plan, q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache,
+                                num_pages, block_table, block_table_stride, seq_lens, softmax_scale,
+                                kv_scale, out, out_dtype, lse, workspace, workspace_bytes, &p);
+  if (st != MLA_OK) return st;
+  p.q_lens = q_lens;
+  if (launch_split_kv(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return mla_combine(plan, out, out_dtype, lse, workspace, workspace_bytes, cuda_stream);
+}
+
 mla_status_t mla_decode_check_error(void* workspace, void* cuda_stream, int32_t info[4]) {
   if (!workspace) return MLA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)cuda_stream;

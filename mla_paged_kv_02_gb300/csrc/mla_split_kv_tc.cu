@@ -320,7 +320,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   const int b = ctl->req;
 
   const int L = lpt ? lens[b] : p.seq_lens[b];
-  const bool len_ok = seq_len_ok(p, L);
+  // This request's query tokens: rows (b, i, h) with i >= qlb are padding of a
+  // per-request q_len call, computed fully masked (out 0, lse -inf).
+  const int qlb = p.q_lens ? p.q_lens[b] : p.q_len;
+  const bool len_ok = qlb >= 1 && qlb <= p.q_len && L >= qlb && L <= p.max_seq_len;
   const int lo = split * p.chunk_tokens;
   const int hi = len_ok ? min(lo + p.chunk_tokens, L) : lo;
   const int first_page = lo / kPage;
@@ -335,7 +338,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   int page_first = 0;
   if (threadIdx.x == 0) {
     ctl->poisoned = len_ok ? 0 : 1;
-    if (!len_ok && split == 0 && rg == 0 && cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, -1, L);
+    if (!len_ok && split == 0 && rg == 0 && cta == 0)
+      report_error(p.err, MLA_ERR_DEVICE_INPUT, b, qlb >= 1 && qlb <= p.q_len ? -1 : -2, qlb >= 1 && qlb <= p.q_len ? L : qlb);
     if (n_pages > 0) {
       page_first = bt_row[0];
       fence_proxy_async_smem();  // the barrier initialisations are visible to the copy engine
@@ -593,9 +597,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // touches nothing.
     const int quad = warp & 3;
     const int r = quad * 32 + lane;              // row within the group (TMEM lane)
-    const bool row_ok = row0 + r < p.rows;
+    const bool row_ok = row0 + r < p.rows;   // the row exists (it is written)
     const int qi = (row0 + r) / p.num_heads;
-    const int vis = L - p.q_len + 1 + qi;        // tokens this row may see
+    const bool row_live = row_ok && qi < qlb;  // not padding of a per-request q_len
+    const int vis = L - qlb + 1 + qi;           // tokens this row may see
     const float sc2 = p.softmax_scale * kv_scale * kLog2e;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t col_own = kColS + 32 * cta;    // S columns of this CTA's token half (within a buffer)
@@ -754,7 +759,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         break;
       }
       const int tok_c = tok0 + 32 * (int)cta;
-      const int n_vis = (page_ok && row_ok) ? min(max(vis - tok_c, 0), 32) : 0;
+      const int n_vis = (page_ok && row_live) ? min(max(vis - tok_c, 0), 32) : 0;
       const bool fast = __all_sync(0xffffffffu, n_vis == 32);
       float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       {

@@ -180,6 +180,54 @@ def test_batch_above_ranking_limit():
     compare(out, lse, ref_o, ref_l, what="B=1100")
 
 
+def _request(inp, b, q_len):
+    """Request b alone with its first q_len query tokens (CPU inputs)."""
+    sub = synth.Inputs(**{**inp.__dict__})
+    sub.batch = 1
+    sub.q_len = q_len
+    sub.q_nope = inp.q_nope[b:b + 1, :q_len].contiguous()
+    sub.q_pe = inp.q_pe[b:b + 1, :q_len].contiguous()
+    sub.block_table = inp.block_table[b:b + 1].contiguous()
+    sub.seq_lens = inp.seq_lens[b:b + 1].contiguous()
+    return sub
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_varlen_q_len(fp8):
+    # Per-request q_len through mla_decode_varlen: each request's live rows
+    # against the oracle on that request alone; padding rows are 0 / -inf.
+    q_lens = [1, 4, 2, 3, 4, 1, 2]
+    kv = [5, 300, 64, 1000, 4, 2000, 130]
+    inp = small(1000 + fp8, 4, kv, H=32, sharp=3.0, kv_fp8=fp8)
+    dev = inp.to("cuda")
+    ql = torch.tensor(q_lens, dtype=torch.int32, device="cuda")
+    refs = [oracle.decode(_request(inp, b, q)) for b, q in enumerate(q_lens)]
+    for s in (0, 1, 3):
+        out, lse, _ = api.decode(dev, force_splits=s, out_fp32=True, q_lens=ql)
+        torch.cuda.synchronize()
+        for b, q in enumerate(q_lens):
+            compare(out[b:b + 1, :q], lse[b:b + 1, :q], refs[b][0], refs[b][1], fp8=fp8,
+                    what=f"varlen splits={s} b={b} q={q}")
+            assert torch.all(out[b, q:] == 0) and torch.all(torch.isneginf(lse[b, q:]))
+
+
+def test_varlen_bad_q_len_is_reported_and_isolated():
+    q_lens = [2, 0, 3, 5]  # 0 and 5 (> the planned 4) are invalid
+    inp = small(1100, 4, [50, 60, 70, 80], H=16)
+    dev = inp.to("cuda")
+    ql = torch.tensor(q_lens, dtype=torch.int32, device="cuda")
+    with pytest.raises(_lib.MlaError) as e:
+        api.decode(dev, out_fp32=True, q_lens=ql)
+    assert e.value.status == _lib.MLA_ERR_DEVICE_INPUT
+    out, lse, _ = api.decode(dev, out_fp32=True, q_lens=ql, check=False)
+    torch.cuda.synchronize()
+    assert torch.isnan(out[1]).all() and torch.isnan(out[3]).all()
+    for b in (0, 2):
+        q = q_lens[b]
+        ref_o, ref_l = oracle.decode(_request(inp, b, q))
+        compare(out[b:b + 1, :q], lse[b:b + 1, :q], ref_o, ref_l, what=f"valid b={b}")
+
+
 def test_split_count_independence():
     inp = small(700, 4, [4, 500, 2000, 4096], H=32, sharp=5.0)
     ref_o, ref_l = oracle.decode(inp)
