@@ -230,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + Lay::kCtlOff);
-  uint8_t* sQ = smem + Lay::kQStageOff;  // Q staging (then stages 2-3)
+  uint8_t* sQ = smem + Lay::kQStageOff;  // Q staging (then the ring's last two stages)
   uint8_t* sKV = smem + kStageOff;
   uint8_t* sSin = smem + Lay::kSinOff;
   uint8_t* sQpe = smem + Lay::kQpeOff;
