@@ -142,6 +142,7 @@ struct Ctl {
   uint64_t pv_ready[2];        // local P halves written (count 4) + the peer's halves landed
   uint64_t u_ready[2];         // the peer's references for the page landed (count 4 + 512 B)
   uint64_t checked[2];         // the 4 local warps ran the page's reference check (count 4)
+  uint64_t p_recv[4];          // per quadrant: the peer holds this CTA's P rows it had to scale (count 1, remote)
   uint64_t fin;                // the peer's row sums delivered (count 4 + 512 B)
   uint64_t drain;
   uint32_t tmem_base;
@@ -267,6 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     for (int q = 0; q < 4; ++q) {
       mbar_init(&ctl->sin_full[q], 1);
       mbar_init(&ctl->sin_free[q], 1);
+      mbar_init(&ctl->p_recv[q], 1);
     }
     for (int e = 0; e < 2; ++e) {
       mbar_init(&ctl->pv_ready[e], 4);
@@ -610,6 +612,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     float r_ref = -INFINITY;   // reference this CTA computes P with
     float a_ref = -INFINITY;   // reference both CTAs agreed on, through the last checked page
     float l_sum = 0.f;         // exp sum over this CTA's token halves, relative to r_ref
+    int own_fixes = 0;         // pages on which this warp scaled its own P rows (p_recv phases)
     bool poisoned = !len_ok;
     bool ok = true;
 
@@ -649,7 +652,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       const float an = fmaxf(a_ref, fmaxf(u_own, u_oth));
       const bool resc = k > 0 && an > a_ref;  // PV(0) overwrites O
       const bool fix_own = u_own < an, fix_oth = u_oth < an;
-      if (__any_sync(0xffffffffu, resc || fix_own || fix_oth)) {
+      const bool any_own = __any_sync(0xffffffffu, fix_own), any_oth = __any_sync(0xffffffffu, fix_oth);
+      if (__any_sync(0xffffffffu, resc) || any_own || any_oth) {
         if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->pv_ready[e], (k >> 1) & 1, p, 19))) return false;
         if (__any_sync(0xffffffffu, resc)) {
           // O holds exactly pages < k once PV(k-1) has completed.
@@ -671,26 +675,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
           tmem_st_wait();
           tc_fence_before();
         }
-        // P halves computed against a lower reference; the factors are powers of two.
+        // P halves computed against a lower reference; the factors are powers of
+        // two.  The peer's half first: its rows have landed (pv_ready), so the
+        // peer learns that its copy is done with its source and may scale that
+        // half in place.  This CTA's own half was sent to the peer just before
+        // this check; it is scaled in place only once the peer signals the same,
+        // so that the copy never reads half-scaled rows.  Both CTAs take the same
+        // decisions (an, the references and a_ref are equal on both sides).
+        auto scale_half = [&](int h, bool fix, float u) {
+          if (!fix) return;
+          const float f = ex2(u - an);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const bool fix = h == (int)cta ? fix_own : fix_oth;
-          if (fix) {
-            const float f = ex2((h == (int)cta ? u_own : u_oth) - an);
+          for (int uu = 0; uu < 4; ++uu) {
+            uint4* c = reinterpret_cast<uint4*>(p_chunk(k % Lay::kPBufs, 4 * h + uu));
+            uint4 w = *c;
+            uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint4* c = reinterpret_cast<uint4*>(p_chunk(k % Lay::kPBufs, 4 * h + u));
-              uint4 w = *c;
-              uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[i]));
-                __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
-                wv[i] = *reinterpret_cast<uint32_t*>(&y);
-              }
-              *c = w;
+            for (int i = 0; i < 4; ++i) {
+              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[i]));
+              __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
+              wv[i] = *reinterpret_cast<uint32_t*>(&y);
             }
+            *c = w;
           }
+        };
+        if (any_oth) {
+          scale_half((int)peer, fix_oth, u_oth);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&ctl->p_recv[quad]), peer));
+        }
+        if (any_own) {
+          if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->p_recv[quad], own_fixes & 1, p, 23))) return false;
+          ++own_fixes;
+          scale_half((int)cta, fix_own, u_own);
         }
         fence_proxy_async_smem();
       }

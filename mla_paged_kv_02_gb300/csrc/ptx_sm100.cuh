@@ -80,7 +80,8 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_add
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// The same for one 32-bit word (4 transaction bytes).
+// Asynchronous 4-byte store into a peer CTA's shared memory that completes 4
+// transaction bytes on the peer's mbarrier (no release fence needed).
 __device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t v, uint32_t cluster_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr),
                "r"(v), "r"(cluster_bar)
