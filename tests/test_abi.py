@@ -128,3 +128,19 @@ def test_decode_validation_rejects_before_launch(lib):
     bad = _lib.Plan.from_buffer_copy(pl)
     bad.num_kv_splits = 1  # one split of 128 tokens cannot cover max_seq_len 200
     assert _call_decode(lib, bad) == E
+
+
+def test_decode_varlen_validation_rejects_before_launch(lib):
+    # The per-request q_len entry point: a missing q_lens array, and every
+    # host-checkable problem of mla_decode, return before any launch.
+    pl = _lib.plan(2, 16, 4, 200, num_sms=148, force_splits=2)
+    P = ctypes.c_void_p
+    E = _lib.MLA_ERR_INVALID_ARG
+
+    def call(q_lens=0x80000, q_nope=0x10000):
+        return lib.mla_decode_varlen(ctypes.byref(pl), P(q_nope), 512, P(0x20000), 64, P(0x30000), 8,
+                                     P(0x40000), 4, P(0x50000), P(q_lens), 0.07, None, P(0x60000), 0,
+                                     None, P(0x70000), pl.workspace_bytes, None)
+
+    assert call(q_lens=0) == E
+    assert call(q_nope=0) == E
