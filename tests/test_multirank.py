@@ -7,6 +7,7 @@ under gloo, and check that evaluating disjoint request shards on two ranks and
 gathering the results reproduces the single-process answer exactly.
 """
 import os
+import queue
 import socket
 
 import numpy as np
@@ -22,8 +23,10 @@ def _free_port():
 
 
 def _worker(rank, world, port, q):
+    # The CPU path under test: no GPU for the ranks even on a machine that has
+    # one (two ranks on one GPU would also be refused by NCCL).
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
-                      LOCAL_RANK=str(rank))
+                      LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")
     import sys
 
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -72,12 +75,20 @@ def test_two_gloo_ranks():
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
-    for p in procs:
-        p.start()
-    for p in procs:
-        p.join(timeout=240)
-    results = dict(q.get(timeout=5) for _ in range(world))
-    for p in procs:
-        if p.is_alive():
-            p.kill()
+    try:
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=240)
+        results = {}
+        for _ in range(world):
+            try:
+                rank, msg = q.get(timeout=5)
+            except queue.Empty:  # a rank that never reported is a failure below
+                break
+            results[rank] = msg
+    finally:
+        for p in procs:
+            if p.is_alive():
+                p.kill()
     assert results == {0: "ok", 1: "ok"}, results
