@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import torch
@@ -91,11 +92,11 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="mla_bench_clocks_", suffix=".csv")
+        os.close(fd)
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
@@ -127,6 +128,10 @@ class ClockSampler:
                 for n, v in zip(names, parts[5:9]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
@@ -181,24 +186,34 @@ def cpu_baseline(inp, reqs, threads=None):
 
 
 def run_reference(args, world, rank):
-    """Reference arm: the CPU oracle on a bounded sample per step (rank 0 only)."""
+    """Reference arm: the CPU oracle on a bounded sample per step (rank 0 only).
+
+    A whole MTP-3 call takes the fp64 oracle about a minute on 16 cores, so each
+    step evaluates one request of the call (1/64 of its work) and ``value`` is
+    that time scaled to the whole call; ``ms_per_step`` is the time a step
+    really took, so steps x ms_per_step is the wall time of the timed region."""
     if rank != 0:
         return
     from mla_paged_kv_02_gb300 import synth
 
     inp = synth.make_inputs("mtp3", seed=2, device="cpu" if not torch.cuda.is_available() else "cuda")
     reqs = [0]
-    times = []
+    times, step_s = [], []
     for k in range(args.warmup + args.steps):
         us, cores, dt = cpu_baseline(inp, reqs)
         if k >= args.warmup:
             times.append(us)
+            step_s.append(dt)
     v = statistics.mean(times)
-    sample = f"1 of {inp.batch} requests (all {inp.num_heads * inp.q_len} rows x {int(inp.seq_lens[0])} tokens) per step, scaled x{inp.batch}"
+    scale = inp.batch / len(reqs)
+    sample = (f"1 of {inp.batch} requests (all {inp.num_heads * inp.q_len} rows x {int(inp.seq_lens[0])} "
+              f"tokens) per step; value = step time x{scale:g}")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(step_s) * 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
             "config": {"workload": "mtp3: B=64 H=32 q_len=4 kv_len=81920 page=64 bf16 KV, CPU oracle sample"},
+            "extrapolated": {"from_sample_fraction": len(reqs) / inp.batch, "factor": scale},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -18,11 +18,15 @@
  *
  * Row order everywhere: rows are (b, i, h) with flat index (b*q_len + i)*H + h.
  *
- * Ownership: the caller owns every buffer, including the workspace.  The
- * library allocates no device memory, keeps no state between calls and caches
- * no scale (a stale cached scale and a leaked per-device workspace are the two
- * risks the TokenSpeed MLA review flags).  All device work is asynchronous on
- * the caller's stream; no entry point but mla_decode_check_error synchronises.
+ * Ownership: the caller owns every buffer, including the workspace.  Every
+ * entry point except mla_decode_noalloc allocates no device memory, keeps no
+ * state between calls and caches no scale (a stale cached scale and a leaked
+ * per-device workspace are the two risks the TokenSpeed MLA review flags).
+ * mla_decode_noalloc is the one exception: it works in a fixed array that the
+ * library's device image reserves on every GPU that loads it (see its block
+ * below for the size and the sharing rules).  All device work is asynchronous
+ * on the caller's stream; no entry point but mla_decode_check_error
+ * synchronises.
  */
 #ifndef MLA_DECODE_H_
 #define MLA_DECODE_H_
@@ -82,9 +86,16 @@ typedef struct {
  *
  * Splits are chosen so that batch * row_groups * splits CTAs fill whole waves
  * of the SMs while each split keeps enough pages to amortise its set-up, and
- * the partial bytes stay small next to the KV bytes.  Returns
- * MLA_ERR_UNSUPPORTED for page_size != 64 or q_len outside 1..8, and
- * MLA_ERR_INVALID_ARG for non-positive sizes.  Touches no GPU when num_sms > 0.
+ * the partial bytes stay small next to the KV bytes (the TokenSpeed summary,
+ * implementation step 1, sizes its partials from the SM count for the same
+ * reason).  Returns MLA_ERR_UNSUPPORTED for page_size != 64, q_len outside
+ * 1..8, num_heads * q_len > 4096, batch > 65535 (the batch is a grid
+ * dimension) or max_seq_len > 2^30, and MLA_ERR_INVALID_ARG for non-positive
+ * sizes.  Touches no GPU when num_sms > 0.
+ *
+ * Every entry point that takes a plan re-derives its byte counts and split
+ * geometry from its shape and returns MLA_ERR_INVALID_ARG, before any launch,
+ * for a plan that was edited after mla_decode_plan filled it in.
  */
 mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_len, int page_size,
                              mla_kv_dtype_t kv_dtype, int num_sms, int force_splits,
@@ -93,12 +104,20 @@ mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_le
 /*
  * mla_workspace_init -- zero the workspace header (the sticky device error
  * word) once after the caller allocates the workspace.  Asynchronous on stream.
+ * Library plumbing with no counterpart on the source pages: it exists because
+ * the caller, not the library, owns the workspace (the preallocated workspace
+ * of the vLLM PR #46819 summary, implementation breakdown 2).
  */
 mla_status_t mla_workspace_init(void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
  * mla_decode -- the whole decode: the split-KV attention kernel, then (when
- * plan->num_kv_splits > 1) the LSE-weighted combine kernel.
+ * plan->num_kv_splits > 1) the LSE-weighted combine kernel.  The operation is
+ * the absorbed-form decode at the top of this header; the call shape (query
+ * parts, paged cache, block table, lengths, per-call scales, out + lse) is
+ * the TokenSpeed MLA summary's decode interface (vLLM PR #41778,
+ * implementation breakdown 1), with the FP8 dequant scale passed on every
+ * call as its review highlights ask.
  *
  *   q_nope  : bf16 rows (b,i,h), 512 used, row stride q_nope_row_stride elements
  *   q_pe    : bf16 rows (b,i,h), 64 used, row stride q_pe_row_stride elements
@@ -133,8 +152,9 @@ mla_status_t mla_decode(const mla_decode_plan_t* plan, const void* q_nope, int64
 
 /*
  * mla_split_kv -- the first stage alone (paged KV gather, QK^T, online
- * softmax with the causal mask, PV, split epilogue).  Same arguments as
- * mla_decode.  With one split it writes out/lse directly; otherwise it writes
+ * softmax with the causal mask, PV, split epilogue); the per-split partial of
+ * width kv_lora_rank + 1 follows the attn_logits layout of the vLLM PR #46819
+ * summary (key code excerpt).  Same arguments as mla_decode.  With one split it writes out/lse directly; otherwise it writes
  * the fp32 partials [B, q_len, H, splits, 513] (512 normalised outputs, then
  * the split's LSE; an empty split writes 0 and -inf) into the workspace.
  */
@@ -148,7 +168,9 @@ mla_status_t mla_split_kv(const mla_decode_plan_t* plan, const void* q_nope,
 /*
  * mla_combine -- the second stage alone: for every row, M = max_s lse_s,
  * lse = M + ln sum_s exp(lse_s - M), out = sum_s exp(lse_s - lse) * o_s, read
- * from the partials mla_split_kv wrote.  A no-op when the plan has one split.
+ * from the partials mla_split_kv wrote (the split-KV reduction whose partials
+ * carry one LSE per split, vLLM PR #46819 summary, key code excerpt).  A
+ * no-op when the plan has one split.
  */
 mla_status_t mla_combine(const mla_decode_plan_t* plan, void* out, mla_out_dtype_t out_dtype,
                          float* lse, const void* workspace, size_t workspace_bytes,
@@ -195,9 +217,14 @@ mla_status_t mla_decode_varlen(const mla_decode_plan_t* plan, const void* q_nope
  *   - Every call on a device shares the array and it keeps the last call's
  *     contents; calls that may overlap on the GPU race on it, so order them.
  *   - The first call on a device looks up and caches the array's device
- *     address; make it before any stream capture starts.
- *   - The error word is cleared at the start of each call; device-side input
- *     errors show up only as NaN rows of the affected request.
+ *     address; make it before any stream capture starts.  The cached address
+ *     belongs to the device's current context: after cudaDeviceReset it is
+ *     stale, so do not call this entry point again in that process.
+ *   - The error word is cleared at the start of each call and the caller has
+ *     no workspace pointer to read it with, so device-side problems show up
+ *     only in the outputs: an input error (bad seq_len or page index) and a
+ *     bounded wait that ran out (a timeout) both write the affected rows of
+ *     out and lse as NaN.  Callers check the outputs for NaN.
  */
 #define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
 mla_status_t mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q_nope,
@@ -212,10 +239,14 @@ mla_status_t mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q_nop
  * error word from the workspace header, clears it, and returns MLA_OK,
  * MLA_ERR_DEVICE_INPUT or MLA_ERR_TIMEOUT (or MLA_ERR_CUDA if the stream
  * itself failed).  info (may be NULL) receives {code, request, index, value}.
+ * It is how device-side errors surface instead of going unnoticed (the
+ * TokenSpeed MLA summary, risks and impact item 6, warns that a leftover
+ * fallback path can turn a mismatched batch into an out-of-bounds access).
  */
 mla_status_t mla_decode_check_error(void* workspace, void* cuda_stream, int32_t info[4]);
 
-/* Human-readable name of a status code (static storage). */
+/* Human-readable name of a status code (static storage).  Library plumbing;
+ * no passage of the source pages corresponds to it. */
 const char* mla_status_string(mla_status_t status);
 
 #ifdef __cplusplus

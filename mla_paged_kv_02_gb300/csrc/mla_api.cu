@@ -17,18 +17,45 @@ constexpr int kRowsPerCta = 128;
 constexpr int kCtasPerGroup = 2;
 constexpr int kMaxSplits = 256;
 constexpr double kSetupPages = 2.0;
+// The split kernel's grid is (2 * row_groups, splits, batch): the splits and
+// the batch sit on gridDim.y and gridDim.z, whose hardware limit is 65535.
+constexpr int kMaxGridYZ = 65535;
+constexpr int kMaxRows = 4096;  // num_heads * q_len per request
+// Token positions stay far from int32 overflow in split * chunk_tokens + chunk_tokens.
+constexpr int kMaxSeqLen = 1 << 30;
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-bool plan_ok(const mla_decode_plan_t* pl) {
-  return pl && pl->batch >= 1 && pl->num_heads >= 1 && pl->q_len >= 1 &&
-         pl->q_len <= MLA_MAX_Q_LEN && pl->page_size == MLA_PAGE_SIZE && pl->max_seq_len >= pl->q_len &&
-         pl->num_kv_splits >= 1 && pl->chunk_tokens >= MLA_PAGE_SIZE &&
-         pl->chunk_tokens % MLA_PAGE_SIZE == 0 && pl->rows_per_cta == kRowsPerCta &&
-         pl->row_groups == ceil_div((int64_t)pl->num_heads * pl->q_len, kRowsPerCta) &&
-         (pl->kv_dtype == MLA_KV_BF16 || pl->kv_dtype == MLA_KV_FP8_E4M3) &&
-         (int64_t)pl->num_kv_splits * pl->chunk_tokens >= pl->max_seq_len;
+// Bytes of fp32 split partials [batch, q_len, H, splits, 513]; none with one split.
+size_t partial_bytes_for(int64_t batch, int64_t rows, int64_t splits) {
+  return splits > 1 ? (size_t)(batch * rows * splits * (MLA_KV_LORA_RANK + 1)) * sizeof(float) : 0;
 }
+
+// A plan is usable only if every field is the planner's own arithmetic: the
+// kernels size their writes from num_kv_splits, so a plan whose byte counts do
+// not follow from its shape (edited after mla_decode_plan, or never planned)
+// would let the split kernel write past the caller's workspace.
+bool plan_ok(const mla_decode_plan_t* pl) {
+  if (!(pl && pl->batch >= 1 && pl->batch <= kMaxGridYZ && pl->num_heads >= 1 && pl->q_len >= 1 &&
+        pl->q_len <= MLA_MAX_Q_LEN && (int64_t)pl->num_heads * pl->q_len <= kMaxRows &&
+        pl->page_size == MLA_PAGE_SIZE && pl->max_seq_len >= pl->q_len && pl->num_kv_splits >= 1 &&
+        pl->num_kv_splits <= kMaxGridYZ && pl->chunk_tokens >= MLA_PAGE_SIZE &&
+        pl->chunk_tokens % MLA_PAGE_SIZE == 0 && pl->rows_per_cta == kRowsPerCta &&
+        pl->row_groups == ceil_div((int64_t)pl->num_heads * pl->q_len, kRowsPerCta) &&
+        (pl->kv_dtype == MLA_KV_BF16 || pl->kv_dtype == MLA_KV_FP8_E4M3) &&
+        pl->max_seq_len <= kMaxSeqLen && pl->chunk_tokens <= pl->max_seq_len + MLA_PAGE_SIZE - 1 &&
+        (int64_t)pl->num_kv_splits * pl->chunk_tokens >= pl->max_seq_len &&
+        (int64_t)(pl->num_kv_splits - 1) * pl->chunk_tokens < pl->max_seq_len))
+    return false;
+  const size_t part = partial_bytes_for(pl->batch, (int64_t)pl->num_heads * pl->q_len, pl->num_kv_splits);
+  return pl->partial_bytes == part && pl->workspace_bytes == MLA_WORKSPACE_HEADER_BYTES + part;
+}
+
+}  // namespace
+
+bool mla::plan_valid(const mla_decode_plan_t* pl) { return plan_ok(pl); }
+
+namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -100,7 +127,8 @@ mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_le
   if (page_size != MLA_PAGE_SIZE || q_len > MLA_MAX_Q_LEN) return MLA_ERR_UNSUPPORTED;
   if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
   if (max_seq_len < q_len) return MLA_ERR_INVALID_ARG;
-  if ((int64_t)num_heads * q_len > 4096) return MLA_ERR_UNSUPPORTED;
+  if ((int64_t)num_heads * q_len > kMaxRows || batch > kMaxGridYZ || max_seq_len > kMaxSeqLen)
+    return MLA_ERR_UNSUPPORTED;
   if (num_sms <= 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -117,6 +145,7 @@ mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_le
   int splits = 1;
   if (force_splits > 0) {
     splits = force_splits < pages ? force_splits : pages;
+    if (splits > kMaxGridYZ) splits = kMaxGridYZ;
   } else {
     // Smallest modelled time: whole waves of one-CTA-per-SM work, each CTA paying
     // its pages plus a fixed set-up, plus the partial write+read (and combine launch)
@@ -152,8 +181,7 @@ mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_le
   plan->chunk_tokens = chunk_pages * MLA_PAGE_SIZE;
   plan->rows_per_cta = kRowsPerCta;
   plan->row_groups = row_groups;
-  plan->partial_bytes =
-      splits > 1 ? (size_t)batch * rows * splits * (MLA_KV_LORA_RANK + 1) * sizeof(float) : 0;
+  plan->partial_bytes = partial_bytes_for(batch, rows, splits);
   plan->workspace_bytes = MLA_WORKSPACE_HEADER_BYTES + plan->partial_bytes;
   return MLA_OK;
 }

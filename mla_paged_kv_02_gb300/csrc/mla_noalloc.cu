@@ -19,10 +19,14 @@
 //   * The first call on a device looks up the array's device address and caches
 //     it; make that first call before any stream capture begins.
 //   * The error word is cleared at the start of each call, so a device-side input
-//     error is visible only as NaN rows of the affected request.
+//     error or a bounded wait that ran out is visible only as NaN rows of the
+//     affected request.
+//   * The cached address belongs to the device's context; after
+//     cudaDeviceReset it is stale.
 #include <mutex>
 
 #include "common.cuh"
+#include "kernels.h"
 #include "mla_decode.h"
 
 namespace {
@@ -65,7 +69,9 @@ extern "C" mla_status_t mla_decode_noalloc(const mla_decode_plan_t* plan, const 
                                            const int32_t* seq_lens, float softmax_scale,
                                            const float* kv_scale, void* out, mla_out_dtype_t out_dtype,
                                            float* lse, void* cuda_stream) {
-  if (!plan) return MLA_ERR_INVALID_ARG;
+  // The plan is checked before anything touches the GPU: the scratch array's
+  // bounds are only as good as the plan's byte counts.
+  if (!mla::plan_valid(plan)) return MLA_ERR_INVALID_ARG;
   if (plan->workspace_bytes > (size_t)MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   mla_status_t st = scratch_for_current_device(&ws);

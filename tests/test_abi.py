@@ -130,6 +130,36 @@ def test_decode_validation_rejects_before_launch(lib):
     assert _call_decode(lib, bad) == E
 
 
+def test_edited_plan_is_refused_before_launch(lib):
+    # The kernels size their partial writes from num_kv_splits: a plan edited
+    # after mla_decode_plan (more splits, byte counts left alone) must be
+    # refused by every entry point that takes a plan, before any launch.
+    pl = _lib.plan(2, 16, 1, 4096, num_sms=148, force_splits=2)
+    E = _lib.MLA_ERR_INVALID_ARG
+    bad = _lib.Plan.from_buffer_copy(pl)
+    bad.num_kv_splits = 8
+    bad.chunk_tokens = 512
+    assert _call_decode(lib, bad, wsb=1 << 30) == E
+    assert lib.mla_combine(ctypes.byref(bad), ctypes.c_void_p(0x60000), 0, None, ctypes.c_void_p(0x70000),
+                           1 << 30, None) == E
+    P = ctypes.c_void_p
+    assert lib.mla_decode_noalloc(ctypes.byref(bad), P(0x10000), 512, P(0x20000), 64, P(0x30000), 8,
+                                  P(0x40000), 64, P(0x50000), 0.07, None, P(0x60000), 0, None, None) == E
+    for field, value in (("partial_bytes", pl.partial_bytes * 2), ("workspace_bytes", pl.workspace_bytes + 64),
+                         ("row_groups", 2), ("num_kv_splits", 200)):
+        bad = _lib.Plan.from_buffer_copy(pl)
+        setattr(bad, field, value)
+        assert _call_decode(lib, bad, wsb=1 << 30) == E, field
+
+
+def test_plan_rejects_batch_beyond_grid_limit(lib):
+    # The batch is a grid dimension of the split kernel (limit 65535).
+    p = _lib.Plan()
+    assert lib.mla_decode_plan(65536, 16, 1, 100, 64, 0, 148, 0, ctypes.byref(p)) == _lib.MLA_ERR_UNSUPPORTED
+    assert lib.mla_decode_plan(65535, 16, 1, 100, 64, 0, 148, 0, ctypes.byref(p)) == _lib.MLA_OK
+    assert lib.mla_decode_plan(4, 16, 1, (1 << 30) + 1, 64, 0, 148, 0, ctypes.byref(p)) == _lib.MLA_ERR_UNSUPPORTED
+
+
 def test_decode_varlen_validation_rejects_before_launch(lib):
     # The per-request q_len entry point: a missing q_lens array, and every
     # host-checkable problem of mla_decode, return before any launch.

@@ -291,26 +291,39 @@ def test_device_input_errors_are_reported_and_isolated():
 
 # ---------------------------------------------------------------------------
 # Full-size workloads, in the launch configuration the benchmark times (the
-# planner's choice), checked on a seeded sample of requests the oracle can
-# evaluate one by one.
+# planner's split count), with EVERY request checked against the oracle (the
+# whole call takes the fp64 oracle about 5 s for plain and 1-2 min for the
+# 80k MTP shapes on 16 host cores).  Each workload runs on the benchmark's own
+# data and on one structural variant that makes wrong pages, masks or dropped
+# tiles visible at long context (peaked queries, per-page offsets, needles).
+#
+# Beyond the task's bound (which has an absolute 1e-3 floor that is about the
+# size of the signal at 80k tokens, where |out| ~ 0.1/sqrt(L)), the normalised
+# error max|out-ref| / max|ref| is asserted with the bound's own relative
+# coefficient (1e-2 for a bf16 cache, 2e-2 for FP8) and no floor.
 
-FULL = [("plain", {}), ("mtp3", {}), ("mtp7", {}), ("fp8", {}), ("hetero", {}),
-        ("mtp3", dict(page_offset=0.05, sharp=4.0))]
+FULL = [
+    ("plain", {}), ("plain", dict(needle=True)),
+    ("mtp3", {}), ("mtp3", dict(page_offset=0.05, sharp=4.0)),
+    ("mtp7", {}), ("mtp7", dict(sharp=20.0)),
+    ("fp8", {}), ("fp8", dict(sharp=4.0, page_offset=0.05)),
+    ("hetero", {}), ("hetero", dict(needle=True)),
+]
 
 
-@pytest.mark.parametrize("name,kw", FULL, ids=[f"{n}{'-struct' if k else ''}" for n, k in FULL])
-def test_full_size_sampled(name, kw):
+def _full_id(name, kw):
+    return name + ("-" + "-".join(sorted(kw)) if kw else "")
+
+
+@pytest.mark.parametrize("name,kw", FULL, ids=[_full_id(n, k) for n, k in FULL])
+def test_full_size_every_request(name, kw):
     inp = synth.make_inputs(name, seed=list(synth.WORKLOADS).index(name), device="cuda", **kw)
     out, lse, pl = api.decode(inp)
     torch.cuda.synchronize()
-    g = torch.Generator().manual_seed(1234)
-    reqs = sorted(set([0, inp.batch - 1] + torch.randint(0, inp.batch, (2,), generator=g).tolist()))
-    if name == "hetero":  # include the longest request
-        reqs = sorted(set(reqs + [int(inp.seq_lens.argmax())]))
-    sub = synth.subset(inp, reqs)
-    ref_o, ref_l = oracle.decode(sub)
-    idx = torch.tensor(reqs, device="cuda")
-    compare(out[idx], lse[idx], ref_o, ref_l, fp8=inp.kv_fp8,
-            what=f"{name}{kw} splits={pl.num_kv_splits} reqs={reqs}")
-    # properties at every row: finite, lse >= the log of the visible count's lower bound
-    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    host = inp.to("cpu")
+    del inp
+    ref_o, ref_l = oracle.decode(host)
+    norm = compare(out, lse, ref_o, ref_l, fp8=host.kv_fp8,
+                   what=f"{_full_id(name, kw)} B={host.batch} splits={pl.num_kv_splits} (all requests)")
+    rel, _ = bounds(host.kv_fp8)
+    assert norm <= rel, f"normalised error {norm:.3e} > {rel}"

@@ -66,6 +66,25 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row(name, kw, splits, out_fp32
         within_tolerance(out, lse, ref_o, ref_l, fp8=inp.kv_fp8)
 
 
+def test_noalloc_error_of_one_call_does_not_leak_into_the_next():
+    # The caller cannot read the error word, so each call clears it.  A call
+    # with a device-side input error (one seq_len above the planned maximum)
+    # writes that request's rows as NaN; the next, valid call on the same
+    # scratch array must be finite and match mla_decode.
+    inp = synth.make_inputs("tiny", seed=21, device="cuda", kv_lens=[3, 90, 300], q_len=2, batch=3,
+                            num_heads=16)
+    pl = api.plan_for(inp, force_splits=3)
+    bad = synth.Inputs(**{**inp.__dict__})
+    bad.seq_lens = inp.seq_lens.clone()
+    bad.seq_lens[1] = pl.max_seq_len + 1
+    out, lse = run_noalloc(bad, pl, True)
+    assert torch.isnan(out[1]).all() and torch.isnan(lse[1]).all()
+    assert torch.isfinite(out[0]).all() and torch.isfinite(out[2]).all()
+    ref_o, ref_l, _ = api.decode(inp, pl=pl, out_fp32=True)
+    out, lse = run_noalloc(inp, pl, True)
+    within_tolerance(out, lse, ref_o, ref_l)
+
+
 def test_noalloc_refuses_a_plan_larger_than_its_scratch():
     pl = _lib.plan(64, 128, 8, 131072, num_sms=152, force_splits=64)
     assert pl.workspace_bytes > (32 << 20)
