@@ -58,6 +58,10 @@ def _load():
         lib.oracle_mla_decode_unabsorbed.argtypes = [I, I, I, I, P, I, P, P, P, I, D, P, I, P, D,
                                                      P, P, I]
         lib.oracle_mla_decode_unabsorbed.restype = I
+        lib.oracle_mla_decode_range.argtypes = [I, I, I, I, P, P, I, D, P, I, P, D, P, P, P, I]
+        lib.oracle_mla_decode_range.restype = I
+        lib.oracle_lse_merge.argtypes = [ctypes.c_int64, I, P, P, P]
+        lib.oracle_lse_merge.restype = None
         lib.oracle_bf16_array_to_double.argtypes = [P, P, ctypes.c_int64]
         lib.oracle_e4m3_array_to_double.argtypes = [P, P, ctypes.c_int64]
         _lib = lib
@@ -159,4 +163,34 @@ def decode_unabsorbed(inp, q_orig: np.ndarray, w_uk: np.ndarray, threads: Option
         threads or default_threads())
     if rc:
         raise ValueError(f"oracle_mla_decode_unabsorbed rejected its arguments (code {rc})")
+    return out, lse
+
+
+def decode_range(inp, range_lo: Sequence[int], range_hi: Sequence[int], threads: Optional[int] = None):
+    """Token-range (sequence shard) form: every row (b, i, h) attends to the positions of
+    [range_lo[b], range_hi[b]) it may see.  Returns partials [B, q, H, 513] (512
+    normalised outputs, then the range's LSE; an empty range gives 0 and -inf)."""
+    h = _Host(inp)
+    lo = np.ascontiguousarray(np.asarray(range_lo, dtype=np.int32))
+    hi = np.ascontiguousarray(np.asarray(range_hi, dtype=np.int32))
+    assert lo.shape == (h.B,) and hi.shape == (h.B,)
+    part = np.zeros((h.B, h.q_len, h.H, KV_LORA_RANK + 1))
+    rc = _load().oracle_mla_decode_range(
+        h.B, h.H, h.q_len, h.ps, _ptr(h.q), _ptr(h.kv), h.kv_fp8, h.kv_scale, _ptr(h.bt),
+        h.bt.shape[1], _ptr(h.seq), h.scale, _ptr(lo), _ptr(hi), _ptr(part),
+        threads or default_threads())
+    if rc:
+        raise ValueError(f"oracle_mla_decode_range rejected its arguments (code {rc})")
+    return part
+
+
+def lse_merge(parts: np.ndarray):
+    """LSE merge of partials stacked shard-major, parts [R, ..., 513] -> (out [..., 512], lse [...])."""
+    parts = np.ascontiguousarray(parts, dtype=np.float64)
+    R = parts.shape[0]
+    lead = parts.shape[1:-1]
+    rows = int(np.prod(lead)) if lead else 1
+    out = np.zeros(lead + (KV_LORA_RANK,))
+    lse = np.zeros(lead)
+    _load().oracle_lse_merge(rows, R, _ptr(parts), _ptr(out), _ptr(lse))
     return out, lse

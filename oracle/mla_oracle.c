@@ -88,6 +88,9 @@ typedef struct {
     /* split form only */
     int num_splits, chunk_tokens;
     double* part;               /* [rows, num_splits, 513] or NULL */
+    /* token-range (sequence shard) form only */
+    const int32_t* range_lo;    /* [B] first absolute position of the range */
+    const int32_t* range_hi;    /* [B] one past the last */
     /* un-absorbed form only */
     const double* q_orig;       /* [B, q_len, H, 128] */
     const double* w_uk;         /* [H, 128, 512] */
@@ -161,6 +164,19 @@ static double attend_range(const job_t* J, int b, int i, int h, int lo, int hi,
     return l;
 }
 
+/* Token-range form for a sequence-sharded (DCP) cache: row (b, i, h) attends
+ * only to the absolute positions [range_lo[b], range_hi[b]) that it may see,
+ * i.e. [range_lo[b], min(range_hi[b], V)).  Writes the range's normalised
+ * output and LSE as one 513-entry partial (an empty range gives o = 0 and
+ * lse = -inf), exactly what one shard contributes before the LSE merge. */
+static void range_row(const job_t* J, int b, int i, int h, double* s, double* x, double* part) {
+    int L = J->seq_lens[b];
+    int V = L - J->q_len + 1 + i;
+    int lo = J->range_lo[b];
+    int hi = J->range_hi[b] < V ? J->range_hi[b] : V;
+    part[KV_LORA] = attend_range(J, b, i, h, lo, hi, s, x, part);
+}
+
 typedef struct {
     job_t* J;
     int tid, nthreads;
@@ -186,6 +202,10 @@ static void* worker(void* arg) {
         int64_t r = ((int64_t)b * J->q_len + i) * J->num_heads + h;
         int L = J->seq_lens[b];
         int V = L - J->q_len + 1 + i;
+        if (J->range_lo) {
+            range_row(J, b, i, h, s, x, J->part + r * (KV_LORA + 1));
+            continue;
+        }
         double* out = J->out + r * KV_LORA;
         if (J->num_splits <= 0) {
             J->lse[r] = attend_range(J, b, i, h, 0, V, s, x, out);
@@ -234,6 +254,8 @@ static int validate(const job_t* J) {
         if (L < J->q_len) return 3;
         int pages = (L + J->page_size - 1) / J->page_size;
         if (pages > J->bt_stride) return 4;
+        if (J->range_lo && (J->range_lo[b] < 0 || J->range_hi[b] < J->range_lo[b] || J->range_hi[b] > L))
+            return 7;
     }
     return 0;
 }
@@ -310,4 +332,54 @@ int oracle_mla_decode_unabsorbed(int batch, int num_heads, int q_len, int page_s
     J.q_orig = q_orig; J.w_uk = w_uk; J.qk_nope = qk_nope;
     J.out = out; J.lse = lse;
     return run(&J, num_threads);
+}
+
+/* Token-range form (one sequence shard): part [rows, 513] per row (b, i, h),
+ * the normalised output over the visible positions of [range_lo[b],
+ * range_hi[b]) followed by that range's LSE. */
+int oracle_mla_decode_range(int batch, int num_heads, int q_len, int page_size, const double* q,
+                            const void* kv, int kv_fp8, double kv_scale,
+                            const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                            double softmax_scale, const int32_t* range_lo, const int32_t* range_hi,
+                            double* part, int num_threads) {
+    if (!range_lo || !range_hi || !part) return 8;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.batch = batch; J.num_heads = num_heads; J.q_len = q_len; J.page_size = page_size;
+    J.q = q; J.kv = kv; J.kv_fp8 = kv_fp8; J.kv_scale = kv_scale;
+    J.block_table = block_table; J.bt_stride = bt_stride; J.seq_lens = seq_lens;
+    J.softmax_scale = softmax_scale;
+    J.range_lo = range_lo; J.range_hi = range_hi; J.part = part;
+    return run(&J, num_threads);
+}
+
+/* LSE merge of R partials per row: parts [R, rows, 513] (shard-major, the
+ * layout an all-gather of per-shard partials produces).  For every row:
+ * M = max_s lse_s, lse = M + ln sum_s exp(lse_s - M),
+ * out = sum_s exp(lse_s - lse) o_s; rows whose partials are all empty get
+ * out = 0 and lse = -inf. */
+void oracle_lse_merge(int64_t rows, int num_parts, const double* parts, double* out, double* lse) {
+    for (int64_t r = 0; r < rows; ++r) {
+        double M = -INFINITY;
+        for (int k = 0; k < num_parts; ++k) {
+            double lk = parts[((int64_t)k * rows + r) * (KV_LORA + 1) + KV_LORA];
+            if (lk > M) M = lk;
+        }
+        double* o = out + r * KV_LORA;
+        for (int d = 0; d < KV_LORA; ++d) o[d] = 0.0;
+        if (M == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double acc = 0.0;
+        for (int k = 0; k < num_parts; ++k)
+            acc += exp(parts[((int64_t)k * rows + r) * (KV_LORA + 1) + KV_LORA] - M);
+        double l = M + log(acc);
+        for (int k = 0; k < num_parts; ++k) {
+            const double* pk = parts + ((int64_t)k * rows + r) * (KV_LORA + 1);
+            double w = exp(pk[KV_LORA] - l);
+            for (int d = 0; d < KV_LORA; ++d) o[d] += w * pk[d];
+        }
+        lse[r] = l;
+    }
 }

@@ -229,3 +229,109 @@ def test_rejects_short_sequences():
     inp.seq_lens[0] = 3  # L < q_len
     with pytest.raises(ValueError):
         oracle.decode(inp)
+
+
+# ---------------------------------------------------------------------------
+# Token-range (sequence shard) form and the LSE merge of shard partials: the
+# decode-context-parallel reading of the Triton MLA and sparse-MLA summaries
+# (vLLM PR #46819 key code excerpt, q_num_heads = num_heads * dcp_world_size;
+# vLLM PR #47327, implementation breakdown 1, DCP-aware workspace), where each
+# rank attends over its own token range and the ranks' partials are merged.
+
+def _sdpa_on_range(inp, lo, hi):
+    """torch float64 SDPA / logsumexp of every row restricted to the positions of
+    [lo[b], hi[b]) it may see; rows with nothing to see give 0 / -inf."""
+    B, q, H = inp.batch, inp.q_len, inp.num_heads
+    out = np.zeros((B, q, H, 512))
+    lse = np.full((B, q, H), -np.inf)
+    Q = torch.cat([inp.q_nope, inp.q_pe], dim=-1).to(torch.float64)
+    for b in range(B):
+        L = int(inp.seq_lens[b])
+        X = gather_rows_torch(inp, b, L)
+        for i in range(q):
+            t = torch.arange(L)
+            mask = (t < L - q + 1 + i) & (t >= lo[b]) & (t < hi[b])
+            if not bool(mask.any()):
+                continue
+            qi = Q[b, i]
+            o = F.scaled_dot_product_attention(
+                qi[None, :, None, :], X[None, None].expand(1, H, L, 576),
+                X[None, None, :, :512].expand(1, H, L, 512),
+                attn_mask=mask[None, None, None, :], scale=inp.softmax_scale)
+            out[b, i] = o[0, :, 0].numpy()
+            s = (qi @ X.T) * inp.softmax_scale
+            lse[b, i] = torch.logsumexp(s.masked_fill(~mask[None, :], -math.inf), dim=-1).numpy()
+    return out, lse
+
+
+def test_range_form_matches_torch_sdpa_on_the_range():
+    inp = small(seed=20, q_len=4, kv_lens=(4, 70, 200, 129), B=4)
+    lo, hi = [0, 10, 64, 100], [4, 69, 190, 129]  # row-dependent visibility cuts inside some ranges
+    part = oracle.decode_range(inp, lo, hi)
+    ref_o, ref_l = _sdpa_on_range(inp, lo, hi)
+    assert np.max(np.abs(part[..., :512] - ref_o)) <= 1e-12
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(part[..., 512]), fin)
+    assert np.max(np.abs(part[..., 512][fin] - ref_l[fin])) <= 1e-12
+
+
+@pytest.mark.parametrize("cuts", [(1,), (2,), (3,), (4,)])
+def test_ranges_tiling_the_sequence_merge_to_the_single_pass(cuts):
+    R = cuts[0]
+    inp = small(seed=21 + R, q_len=4, kv_lens=(4, 65, 300, 131), B=4, sharp=3.0)
+    out, lse = oracle.decode(inp)
+    g = np.random.default_rng(R)
+    parts = []
+    bounds = []
+    for b in range(inp.batch):
+        L = int(inp.seq_lens[b])
+        inner = np.sort(g.integers(0, L + 1, size=R - 1))  # ragged, possibly empty pieces
+        bounds.append(np.concatenate([[0], inner, [L]]).astype(int))
+    for k in range(R):
+        lo = [int(bounds[b][k]) for b in range(inp.batch)]
+        hi = [int(bounds[b][k + 1]) for b in range(inp.batch)]
+        parts.append(oracle.decode_range(inp, lo, hi))
+    o2, l2 = oracle.lse_merge(np.stack(parts))
+    assert np.max(np.abs(o2 - out)) <= 1e-12
+    assert np.max(np.abs(l2 - lse)) <= 1e-12
+    # the shard order does not matter
+    o3, l3 = oracle.lse_merge(np.stack(parts[::-1]))
+    assert np.max(np.abs(o3 - o2)) <= 1e-14 and np.max(np.abs(l3 - l2)) <= 1e-13
+
+
+def test_whole_range_is_the_single_pass_bitwise():
+    inp = small(seed=26, q_len=2, kv_lens=(2, 77, 140))
+    out, lse = oracle.decode(inp)
+    part = oracle.decode_range(inp, [0] * inp.batch, [int(x) for x in inp.seq_lens])
+    np.testing.assert_array_equal(part[..., :512], out)
+    np.testing.assert_array_equal(part[..., 512], lse)
+
+
+def test_range_closed_forms():
+    inp = small(seed=27, q_len=2, kv_lens=(2, 50, 100))
+    L = [int(x) for x in inp.seq_lens]
+    # one visible token t = L - 2 (seen by both query rows): out = its c_kv, lse = its score
+    lo = [x - 2 for x in L]
+    hi = [x - 1 for x in L]
+    part = oracle.decode_range(inp, lo, hi)
+    Q = torch.cat([inp.q_nope, inp.q_pe], -1).double().numpy()
+    for b in range(inp.batch):
+        x = gather_rows_torch(inp, b, L[b])[L[b] - 2].numpy()
+        for i in range(inp.q_len):
+            np.testing.assert_array_equal(part[b, i, :, :512], np.broadcast_to(x[:512], (inp.num_heads, 512)))
+            np.testing.assert_allclose(part[b, i, :, 512], inp.softmax_scale * (Q[b, i] @ x), rtol=0, atol=1e-12)
+    # the last position, L - 1, is visible to query row q_len-1 only: row 0 is empty
+    part = oracle.decode_range(inp, [x - 1 for x in L], L)
+    assert np.all(np.isneginf(part[:, 0, :, 512])) and np.all(part[:, 0, :, :512] == 0)
+    assert np.all(np.isfinite(part[:, 1, :, 512]))
+    # merging nothing but empty partials gives 0 / -inf
+    o, l = oracle.lse_merge(np.stack([part[:, :1], part[:, :1]]))
+    assert np.all(o == 0) and np.all(np.isneginf(l))
+
+
+def test_range_rejects_ranges_outside_the_sequence():
+    inp = small(seed=28, q_len=1, kv_lens=(5, 60))
+    with pytest.raises(ValueError):
+        oracle.decode_range(inp, [0, 10], [6, 60])  # past L for request 0
+    with pytest.raises(ValueError):
+        oracle.decode_range(inp, [3, 10], [2, 60])  # hi < lo
