@@ -202,6 +202,54 @@ mla_status_t mla_decode_varlen(const mla_decode_plan_t* plan, const void* q_nope
                                size_t workspace_bytes, void* cuda_stream);
 
 /*
+ * mla_decode_shard -- one rank's part of a decode whose cache is sharded by
+ * sequence across ranks (decode context parallelism: each rank holds a
+ * contiguous range of every request's tokens and attends over it with all
+ * query heads, and the ranks' partial outputs are merged by LSE; the vLLM PR
+ * #46819 summary reserves its split partials for num_heads * dcp_world_size
+ * query heads in the key code excerpt, and the vLLM PR #47327 report makes
+ * its workspace DCP-aware in implementation breakdown 1).
+ *
+ * Same arguments as mla_decode, except:
+ *   kv_cache, block_table : this rank's own paged cache; local token t of
+ *             request b is absolute position shard_start[b] + t and lives at
+ *             block_table[b, t / 64], slot t % 64
+ *   shard_lens  : int32 [batch] on the device, tokens of request b this rank
+ *             holds (0 allowed); plan->max_seq_len >= every shard_lens[b]
+ *   shard_start : int32 [batch] on the device, absolute position of the
+ *             rank's first token of request b
+ *   seq_lens    : int32 [batch] on the device, the whole length L_b of request
+ *             b (the q_len new tokens included): query i sees absolute
+ *             positions [0, L_b - q_len + i], so the mask stays causal
+ *   shard_partial : fp32 [batch, q_len, H, 513], 4-byte aligned: per query row
+ *             the normalised output over the positions it sees in this shard,
+ *             then that part's natural-log LSE (0 and -inf if it sees none)
+ * A request with shard_start < 0, shard_start + shard_lens > L_b or
+ * L_b < q_len is a device-side input error (index -3 or -1) and its rows are
+ * written as NaN.
+ */
+mla_status_t mla_decode_shard(const mla_decode_plan_t* plan, const void* q_nope,
+                              int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                              const void* kv_cache, int num_pages, const int32_t* block_table,
+                              int block_table_stride, const int32_t* shard_lens,
+                              const int32_t* shard_start, const int32_t* seq_lens, float softmax_scale,
+                              const float* kv_scale, float* shard_partial, void* workspace,
+                              size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * mla_combine_shards -- the LSE merge of the shards' partials (the same merge
+ * as mla_combine, over ranks instead of splits).
+ *   rows           : batch * q_len * H
+ *   shard_partials : fp32 [num_shards, rows, 513], shard-major (what an
+ *                    all-gather of every rank's shard_partial produces)
+ *   out, lse       : as for mla_decode ([rows, 512] and [rows])
+ * Rows whose shards are all empty get out = 0 and lse = -inf; a NaN LSE in any
+ * shard (a rejected request) makes the row NaN.
+ */
+mla_status_t mla_combine_shards(int64_t rows, int num_shards, const float* shard_partials, void* out,
+                                mla_out_dtype_t out_dtype, float* lse, void* cuda_stream);
+
+/*
  * mla_decode_noalloc -- mla_decode for callers that cannot allocate device
  * memory (code running inside a host framework that owns every device
  * allocation, or a plug-in handed only input/output pointers).  No counterpart

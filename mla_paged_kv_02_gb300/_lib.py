@@ -38,6 +38,8 @@ EXPORTED = (
     "mla_decode_check_error",
     "mla_decode_noalloc",
     "mla_decode_varlen",
+    "mla_decode_shard",
+    "mla_combine_shards",
     "mla_status_string",
 )
 
@@ -93,6 +95,8 @@ def load() -> ctypes.CDLL:
     lib.mla_decode_check_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.mla_decode_noalloc.argtypes = [PP, P, I64, P, I64, P, I, P, I, P, F, P, P, I, P, P]
     lib.mla_decode_varlen.argtypes = [PP, P, I64, P, I64, P, I, P, I, P, P, F, P, P, I, P, P, SZ, P]
+    lib.mla_decode_shard.argtypes = [PP, P, I64, P, I64, P, I, P, I, P, P, P, F, P, P, P, SZ, P]
+    lib.mla_combine_shards.argtypes = [I64, I, P, P, I, P, P]
     lib.mla_status_string.argtypes = [I]
     lib.mla_status_string.restype = ctypes.c_char_p
     for name in EXPORTED:
@@ -184,3 +188,22 @@ def decode_noalloc(pl: Plan, q_nope, q_pe, kv_cache, block_table, seq_lens, soft
         kv_cache.shape[0], _ptr(block_table), block_table.stride(0), _ptr(seq_lens), float(softmax_scale),
         _ptr(kv_scale), _ptr(out), MLA_OUT_FP32 if out.dtype == torch.float32 else MLA_OUT_BF16, _ptr(lse),
         _stream(stream))
+
+
+def decode_shard(pl: Plan, q_nope, q_pe, kv_cache, block_table, shard_lens, shard_start, seq_lens,
+                 softmax_scale, kv_scale, shard_partial, workspace, stream=None) -> int:
+    """mla_decode_shard: this rank's (o, lse) partial [B, q, H, 513] over its token range."""
+    return load().mla_decode_shard(
+        ctypes.byref(pl), _ptr(q_nope), q_nope.stride(-2), _ptr(q_pe), q_pe.stride(-2), _ptr(kv_cache),
+        kv_cache.shape[0], _ptr(block_table), block_table.stride(0), _ptr(shard_lens), _ptr(shard_start),
+        _ptr(seq_lens), float(softmax_scale), _ptr(kv_scale), _ptr(shard_partial), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def combine_shards(shard_partials, out, lse, stream=None) -> int:
+    """mla_combine_shards: merge [R, rows..., 513] shard partials into out / lse."""
+    R = shard_partials.shape[0]
+    rows = shard_partials[0].numel() // 513
+    return load().mla_combine_shards(rows, R, _ptr(shard_partials), _ptr(out),
+                                     MLA_OUT_FP32 if out.dtype == torch.float32 else MLA_OUT_BF16, _ptr(lse),
+                                     _stream(stream))

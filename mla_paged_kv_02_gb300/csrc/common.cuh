@@ -30,14 +30,25 @@ struct DecodeParams {
   int kv_fp8;
   const int32_t* block_table;
   int bt_stride;
-  const int32_t* seq_lens;
+  const int32_t* seq_lens;  // [B] tokens of request b in this cache (a shard's own count under DCP)
   const int32_t* q_lens;  // [B] per-request number of query tokens (1..q_len), or nullptr: all q_len
+  // Sequence shard (DCP): absolute position of this cache's first token of
+  // request b, and the request's whole length (the causal mask is on absolute
+  // positions).  nullptr: the cache holds the whole request from position 0.
+  const int32_t* kv_start;
+  const int32_t* total_lens;
   float softmax_scale;
   const float* kv_scale;  // device scalar or nullptr
-  void* out;              // [B*R, 512] bf16 or fp32
+  void* out;              // [B*R rows] of 512 bf16 or fp32, out_stride elements apart
   int out_fp32;
-  float* lse;       // [B*R] or nullptr
+  int64_t out_stride;     // 512, or 513 when out/lse are the two parts of a 513-wide partial row
+  float* lse;       // [B*R] lse_stride apart, or nullptr
+  int64_t lse_stride;
   float* partials;  // [B*R, splits, 513] fp32 (splits > 1)
+  // Combine only: element distance between rows and between splits of the
+  // partials it reads ([rows, splits, 513] in the workspace; [splits, rows, 513]
+  // for gathered shard partials).
+  int64_t part_row_stride, part_split_stride;
   int32_t* err;     // workspace header
   int batch, num_heads, q_len, rows;  // rows = num_heads * q_len per request
   int max_seq_len, splits, chunk_tokens, rows_per_cta, row_groups;
@@ -58,17 +69,11 @@ __device__ __forceinline__ void report_error(int32_t* err, int code, int request
   }
 }
 
-// Request-level validity check shared by the attention kernels: the length
-// must cover the q_len new tokens and stay within the planned maximum.
-__device__ __forceinline__ bool seq_len_ok(const DecodeParams& p, int L) {
-  return L >= p.q_len && L <= p.max_seq_len;
-}
-
 __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t row, int d, float v) {
   if (p.out_fp32)
-    reinterpret_cast<float*>(p.out)[row * kKvLora + d] = v;
+    reinterpret_cast<float*>(p.out)[row * p.out_stride + d] = v;
   else
-    reinterpret_cast<__nv_bfloat16*>(p.out)[row * kKvLora + d] = __float2bfloat16_rn(v);
+    reinterpret_cast<__nv_bfloat16*>(p.out)[row * p.out_stride + d] = __float2bfloat16_rn(v);
 }
 
 }  // namespace mla

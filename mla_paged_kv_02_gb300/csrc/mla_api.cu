@@ -94,7 +94,9 @@ mla_status_t fill_params(const mla_decode_plan_t* pl, const void* q_nope, int64_
   p->kv_scale = kv_scale;
   p->out = out;
   p->out_fp32 = out_dtype == MLA_OUT_FP32;
+  p->out_stride = MLA_KV_LORA_RANK;
   p->lse = lse;
+  p->lse_stride = 1;
   p->err = static_cast<int32_t*>(workspace);
   p->partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + MLA_WORKSPACE_HEADER_BYTES);
   p->batch = pl->batch;
@@ -210,9 +212,15 @@ mla_status_t mla_split_kv(const mla_decode_plan_t* plan, const void* q_nope, int
   return MLA_OK;
 }
 
-mla_status_t mla_combine(const mla_decode_plan_t* plan, void* out, mla_out_dtype_t out_dtype,
-                         float* lse, const void* workspace, size_t workspace_bytes,
-                         void* cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// The combine of the workspace partials into out (row stride out_stride) and
+// lse (stride lse_stride).
+mla_status_t combine_workspace(const mla_decode_plan_t* plan, void* out, mla_out_dtype_t out_dtype,
+                               int64_t out_stride, float* lse, int64_t lse_stride, const void* workspace,
+                               size_t workspace_bytes, void* cuda_stream) {
   if (!plan_ok(plan) || !out || !workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_FP32) return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
@@ -221,7 +229,9 @@ mla_status_t mla_combine(const mla_decode_plan_t* plan, void* out, mla_out_dtype
   memset(&p, 0, sizeof p);
   p.out = out;
   p.out_fp32 = out_dtype == MLA_OUT_FP32;
+  p.out_stride = out_stride;
   p.lse = lse;
+  p.lse_stride = lse_stride;
   p.partials = reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(workspace)) +
                                         MLA_WORKSPACE_HEADER_BYTES);
   p.batch = plan->batch;
@@ -229,6 +239,65 @@ mla_status_t mla_combine(const mla_decode_plan_t* plan, void* out, mla_out_dtype
   p.q_len = plan->q_len;
   p.rows = plan->num_heads * plan->q_len;
   p.splits = plan->num_kv_splits;
+  p.part_row_stride = (int64_t)p.splits * kPartRow;
+  p.part_split_stride = kPartRow;
+  if (launch_combine(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_combine(const mla_decode_plan_t* plan, void* out, mla_out_dtype_t out_dtype,
+                         float* lse, const void* workspace, size_t workspace_bytes,
+                         void* cuda_stream) {
+  return combine_workspace(plan, out, out_dtype, MLA_KV_LORA_RANK, lse, 1, workspace, workspace_bytes,
+                           cuda_stream);
+}
+
+mla_status_t mla_decode_shard(const mla_decode_plan_t* plan, const void* q_nope, int64_t q_nope_row_stride,
+                              const void* q_pe, int64_t q_pe_row_stride, const void* kv_cache, int num_pages,
+                              const int32_t* block_table, int block_table_stride, const int32_t* shard_lens,
+                              const int32_t* shard_start, const int32_t* seq_lens, float softmax_scale,
+                              const float* kv_scale, float* shard_partial, void* workspace,
+                              size_t workspace_bytes, void* cuda_stream) {
+  if (!shard_lens || !shard_start || !seq_lens || !shard_partial || !aligned(shard_partial, 4))
+    return MLA_ERR_INVALID_ARG;
+  DecodeParams p;
+  mla_status_t st = fill_params(plan, q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache, num_pages,
+                                block_table, block_table_stride, shard_lens, softmax_scale, kv_scale,
+                                shard_partial, MLA_OUT_FP32, shard_partial + MLA_KV_LORA_RANK, workspace,
+                                workspace_bytes, &p);
+  if (st != MLA_OK) return st;
+  // One 513-wide fp32 row per query row: the 512 outputs, then the LSE.
+  p.out_stride = kPartRow;
+  p.lse_stride = kPartRow;
+  p.kv_start = shard_start;
+  p.total_lens = seq_lens;
+  if (launch_split_kv(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return combine_workspace(plan, shard_partial, MLA_OUT_FP32, kPartRow, shard_partial + MLA_KV_LORA_RANK,
+                           kPartRow, workspace, workspace_bytes, cuda_stream);
+}
+
+mla_status_t mla_combine_shards(int64_t rows, int num_shards, const float* shard_partials, void* out,
+                                mla_out_dtype_t out_dtype, float* lse, void* cuda_stream) {
+  if (rows < 1 || rows > INT32_MAX || num_shards < 1 || !shard_partials || !out) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_FP32) return MLA_ERR_INVALID_ARG;
+  if (!aligned(shard_partials, 4) || !aligned(out, 4)) return MLA_ERR_INVALID_ARG;
+  DecodeParams p;
+  memset(&p, 0, sizeof p);
+  p.out = out;
+  p.out_fp32 = out_dtype == MLA_OUT_FP32;
+  p.out_stride = MLA_KV_LORA_RANK;
+  p.lse = lse;
+  p.lse_stride = 1;
+  p.partials = const_cast<float*>(shard_partials);
+  p.batch = 1;
+  p.rows = (int)rows;
+  p.splits = num_shards;
+  p.part_row_stride = kPartRow;
+  p.part_split_stride = rows * kPartRow;
   if (launch_combine(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -6,7 +6,10 @@
 //   M   = max_s lse_s
 //   lse = M + ln sum_s exp(lse_s - M)
 //   out = sum_s exp(lse_s - lse) * o_s
-// Empty splits carry lse_s = -inf and weigh zero.  One warp per row; each lane
+// Empty splits carry lse_s = -inf and weigh zero (a row whose splits are all
+// empty, which only a sequence shard can have, gets out = 0 and lse = -inf).
+// The same merge joins the partials of sequence shards gathered from several
+// ranks, read with their own row and split strides.  One warp per row; each lane
 // owns 16 of the 512 output columns, so every load of a split's 2 KB is a fully
 // coalesced 128-byte transaction per lane group.  HBM-bound.
 #include "common.cuh"
@@ -32,13 +35,14 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (row >= (int64_t)p.batch * p.rows) return;
-  const float* part = p.partials + row * p.splits * kPartRow;
+  const float* part = p.partials + row * p.part_row_stride;
+  const int64_t sstride = p.part_split_stride;
 
   // Pass 1: the largest split LSE (NaN marks a request the split kernel rejected).
   float M = -INFINITY;
   bool nan_seen = false;
   for (int s = lane; s < p.splits; s += 32) {
-    const float v = part[(int64_t)s * kPartRow + kKvLora];
+    const float v = part[(int64_t)s * sstride + kKvLora];
     nan_seen |= (v != v);
     M = fmaxf(M, v);
   }
@@ -47,7 +51,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams
 
   float acc = 0.f;
   for (int s = lane; s < p.splits; s += 32) {
-    const float v = part[(int64_t)s * kPartRow + kKvLora];
+    const float v = part[(int64_t)s * sstride + kKvLora];
     acc += (v == -INFINITY) ? 0.f : __expf(v - M);
   }
   acc = warp_sum(acc);
@@ -58,7 +62,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams
   for (int k = 0; k < 16; ++k) o[k] = 0.f;
   if (!nan_seen && M != -INFINITY) {
     for (int s = 0; s < p.splits; ++s) {
-      const float* ps = part + (int64_t)s * kPartRow;
+      const float* ps = part + (int64_t)s * sstride;
       const float v = ps[kKvLora];
       if (v == -INFINITY) continue;
       const float w = __expf(v - lse);
@@ -71,7 +75,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams
   }
 #pragma unroll
   for (int k = 0; k < 16; ++k) store_out(p, row, lane + 32 * k, o[k]);
-  if (p.lse && lane == 0) p.lse[row] = lse;
+  if (p.lse && lane == 0) p.lse[row * p.lse_stride] = lse;
 }
 
 }  // namespace

@@ -321,11 +321,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   __syncthreads();
   const int b = ctl->req;
 
-  const int L = lpt ? lens[b] : p.seq_lens[b];
+  const int L = lpt ? lens[b] : p.seq_lens[b];  // tokens of request b in this cache
   // This request's query tokens: rows (b, i, h) with i >= qlb are padding of a
   // per-request q_len call, computed fully masked (out 0, lse -inf).
   const int qlb = p.q_lens ? p.q_lens[b] : p.q_len;
-  const bool len_ok = qlb >= 1 && qlb <= p.q_len && L >= qlb && L <= p.max_seq_len;
+  // A sequence shard holds positions [kv0, kv0 + L) of a request of length
+  // Ltot (possibly none of them); otherwise the cache holds [0, L) and Ltot = L.
+  const bool shard = p.kv_start != nullptr;
+  const int kv0 = shard ? p.kv_start[b] : 0;
+  const int Ltot = shard ? p.total_lens[b] : L;
+  const bool q_ok = qlb >= 1 && qlb <= p.q_len;
+  const bool range_ok = kv0 >= 0 && L >= 0 && (int64_t)kv0 + L <= Ltot;
+  const bool len_ok = q_ok && range_ok && Ltot >= qlb && L <= p.max_seq_len;
   const int lo = split * p.chunk_tokens;
   const int hi = len_ok ? min(lo + p.chunk_tokens, L) : lo;
   const int first_page = lo / kPage;
@@ -340,8 +347,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   int page_first = 0;
   if (threadIdx.x == 0) {
     ctl->poisoned = len_ok ? 0 : 1;
-    if (!len_ok && split == 0 && rg == 0 && cta == 0)
-      report_error(p.err, MLA_ERR_DEVICE_INPUT, b, qlb >= 1 && qlb <= p.q_len ? -1 : -2, qlb >= 1 && qlb <= p.q_len ? L : qlb);
+    if (!len_ok && split == 0 && rg == 0 && cta == 0)  // index -2: q_len, -3: shard range, -1: length
+      report_error(p.err, MLA_ERR_DEVICE_INPUT, b, !q_ok ? -2 : (!range_ok ? -3 : -1),
+                   !q_ok ? qlb : (!range_ok ? kv0 : L));
     if (n_pages > 0) {
       page_first = bt_row[0];
       fence_proxy_async_smem();  // the barrier initialisations are visible to the copy engine
@@ -602,7 +610,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     const bool row_ok = row0 + r < p.rows;   // the row exists (it is written)
     const int qi = (row0 + r) / p.num_heads;
     const bool row_live = row_ok && qi < qlb;  // not padding of a per-request q_len
-    const int vis = L - qlb + 1 + qi;           // tokens this row may see
+    const int vis = Ltot - qlb + 1 + qi - kv0;  // tokens of this cache the row may see
     const float sc2 = p.softmax_scale * kv_scale * kLog2e;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t col_own = kColS + 32 * cta;    // S columns of this CTA's token half (within a buffer)
@@ -929,7 +937,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     if (cta == 0 && row_ok) {
       const float lv = bad ? NAN : (has ? (r_ref + lg2(l_tot)) * kLn2 : -INFINITY);
       if (p.splits == 1) {
-        if (p.lse) p.lse[grow0 + r] = lv;
+        if (p.lse) p.lse[(grow0 + r) * p.lse_stride] = lv;
       } else {
         p.partials[((grow0 + r) * p.splits + split) * kPartRow + kKvLora] = lv;
       }
@@ -989,15 +997,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         for (int rr = 0; rr < 32; ++rr)
           if (rr < nr) dst[rr * step] = col[rr];
       } else if (p.out_fp32) {
-        float* dst = reinterpret_cast<float*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
+        float* dst = reinterpret_cast<float*>(p.out) + (grow0 + quad * 32) * p.out_stride + dim;
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr)
-          if (rr < nr) dst[rr * kKvLora] = col[rr];
+          if (rr < nr) dst[rr * p.out_stride] = col[rr];
       } else {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (grow0 + quad * 32) * p.out_stride + dim;
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr)
-          if (rr < nr) dst[rr * kKvLora] = __float2bfloat16_rn(col[rr]);
+          if (rr < nr) dst[rr * p.out_stride] = __float2bfloat16_rn(col[rr]);
       }
     }
     tc_fence_before();
