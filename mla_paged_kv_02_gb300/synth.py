@@ -10,8 +10,9 @@ Recipe (one ``torch.Generator`` seeded per case; draws in this order):
      sum_b ceil(L_b / page_size) pages (plus spare pages when requested);
   3. the latent cache, fp32 ~ N(0, 0.1^2) rounded to bf16 (RNE), or quantised to
      FP8-E4M3 with one per-tensor scale amax/448;
-  4. q_nope ~ N(0, 1) -> bf16;
-  5. q_pe ~ N(0, 1) -> bf16.
+  4. q_nope ~ N(0, 1) -> bf16 (or, for an FP8 query, E4M3 with one scale
+     amax/448 shared with q_pe);
+  5. q_pe ~ N(0, 1) -> bf16 (or E4M3).
 The block table is ``[B, ceil(max_L / page_size)]`` int32, padded with -1.
 
 Workload shapes follow the vLLM MLA decode microbenchmarks the TokenSpeed MLA
@@ -80,6 +81,8 @@ class Inputs:
     seq_lens: torch.Tensor  # [B] int32
     softmax_scale: float = SOFTMAX_SCALE
     out_fp32: bool = False
+    q_fp8: bool = False  # q_nope / q_pe hold e4m3 codes (uint8); query = code * q_scale
+    q_scale: float = 1.0
 
     @property
     def num_pages(self) -> int:
@@ -139,6 +142,7 @@ def make_inputs(
     kv_fp8: Optional[bool] = None,
     batch: Optional[int] = None,
     num_heads: Optional[int] = None,
+    q_fp8: bool = False,
 ) -> Inputs:
     """Build one seeded decode problem.
 
@@ -149,6 +153,8 @@ def make_inputs(
                      visible token carries c_kv = 32*u_b, so it dominates;
       nan_tail    -- fill slots past L in last pages and all spare pages with NaN;
       spare_pages -- extra pool pages that no request references.
+    q_fp8 quantises the query (q_nope and q_pe together) to FP8-E4M3 with one
+    per-tensor scale amax/448, after the same draws.
     """
     if isinstance(wl, str):
         wl = WORKLOADS[wl]
@@ -195,8 +201,10 @@ def make_inputs(
             sgn = torch.randint(0, 2, (pool,), generator=gen, device=dev).to(torch.float32) * 2 - 1
             kv[:, :, :KV_LORA_RANK] += (page_offset * sgn).to(torch.bfloat16)[:, None, None]
 
-    q_nope = (torch.randn((B, q, H, KV_LORA_RANK), generator=gen, device=dev) * sharp).to(torch.bfloat16)
-    q_pe = (torch.randn((B, q, H, QK_ROPE_DIM), generator=gen, device=dev) * sharp).to(torch.bfloat16)
+    qn32 = torch.randn((B, q, H, KV_LORA_RANK), generator=gen, device=dev) * sharp
+    qp32 = torch.randn((B, q, H, QK_ROPE_DIM), generator=gen, device=dev) * sharp
+    q_nope = qn32.to(torch.bfloat16)
+    q_pe = qp32.to(torch.bfloat16)
 
     bt_dev = bt.to(dev)
     if needle:
@@ -206,6 +214,7 @@ def make_inputs(
             u = torch.randn(KV_LORA_RANK, generator=cpu_gen, dtype=torch.float32)
             u = (u / u.norm()).to(dev)
             q_nope[b] = (q_nope[b].float() + 8.0 * u).to(torch.bfloat16)
+            qn32[b] += 8.0 * u
             page, slot = int(bt[b, t // ps]), t % ps
             row = 32.0 * u
             if wl.kv_fp8:
@@ -231,6 +240,14 @@ def make_inputs(
             else:
                 kv[spare] = float("nan")
 
+    q_scale = 1.0
+    if q_fp8:
+        amax = max(float(qn32.abs().max().item()), float(qp32.abs().max().item())) if qn32.numel() else 1.0
+        q_scale = amax / E4M3_MAX if amax > 0 else 1.0
+        q_nope = (qn32 / q_scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+        q_pe = (qp32 / q_scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+    del qn32, qp32
+
     return Inputs(
         batch=B,
         num_heads=H,
@@ -244,6 +261,8 @@ def make_inputs(
         block_table=bt_dev,
         seq_lens=torch.tensor(lens, dtype=torch.int32, device=dev),
         out_fp32=wl.out_fp32,
+        q_fp8=q_fp8,
+        q_scale=float(q_scale),
     )
 
 
@@ -287,4 +306,4 @@ def subset(inp: Inputs, reqs) -> Inputs:
                   page_size=inp.page_size, q_nope=inp.q_nope[idx].cpu(), q_pe=inp.q_pe[idx].cpu(),
                   kv_cache=kv, kv_fp8=inp.kv_fp8, kv_scale=inp.kv_scale, block_table=bt,
                   seq_lens=torch.tensor(lens, dtype=torch.int32), softmax_scale=inp.softmax_scale,
-                  out_fp32=inp.out_fp32)
+                  out_fp32=inp.out_fp32, q_fp8=inp.q_fp8, q_scale=inp.q_scale)

@@ -62,6 +62,8 @@ def _load():
         lib.oracle_mla_decode_range.restype = I
         lib.oracle_lse_merge.argtypes = [ctypes.c_int64, I, P, P, P]
         lib.oracle_lse_merge.restype = None
+        lib.oracle_e4m3_encode_array.argtypes = [P, P, ctypes.c_int64]
+        lib.oracle_e4m3_encode_array.restype = None
         lib.oracle_bf16_array_to_double.argtypes = [P, P, ctypes.c_int64]
         lib.oracle_e4m3_array_to_double.argtypes = [P, P, ctypes.c_int64]
         _lib = lib
@@ -94,15 +96,34 @@ def e4m3_to_f64(codes: torch.Tensor | np.ndarray) -> np.ndarray:
     return out
 
 
+def e4m3_encode(x) -> np.ndarray:
+    """Round float64 values to OCP E4M3 codes (nearest, ties to even, saturating to
+    +-448) with the C encoder."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def query_f64(inp) -> np.ndarray:
+    """[B, q, H, 576] float64 query rows q_nope | q_pe: bf16 values, or, for an FP8
+    query, e4m3 codes times the per-tensor q_scale (decoded by the C decoder)."""
+    if getattr(inp, "q_fp8", False):
+        qn = e4m3_to_f64(inp.q_nope) * float(inp.q_scale)
+        qp = e4m3_to_f64(inp.q_pe) * float(inp.q_scale)
+    else:
+        qn = bf16_to_f64(inp.q_nope)
+        qp = bf16_to_f64(inp.q_pe)
+    return np.concatenate([qn, qp], axis=-1)
+
+
 class _Host:
     """Host (numpy) views of an input problem, restricted to what the oracle reads."""
 
     def __init__(self, inp, q: Optional[np.ndarray] = None):
         self.B, self.H, self.q_len, self.ps = inp.batch, inp.num_heads, inp.q_len, inp.page_size
         if q is None:
-            qn = bf16_to_f64(inp.q_nope)
-            qp = bf16_to_f64(inp.q_pe)
-            q = np.concatenate([qn, qp], axis=-1)
+            q = query_f64(inp)
         self.q = np.ascontiguousarray(q, dtype=np.float64)
         kv = inp.kv_cache.detach().cpu().contiguous()
         if inp.kv_fp8:

@@ -65,6 +65,32 @@ double oracle_e4m3_to_double(uint8_t byte) {
     return s ? -v : v;
 }
 
+/* double -> OCP FP8 E4M3 (e4m3fn) code: round to nearest, ties to even, on the
+ * e4m3 grid (spacing 2^(E-3) in binade [2^E, 2^(E+1)) for E >= -6, and the
+ * subnormal spacing 2^-9 below 2^-6); magnitudes of 448 and beyond (and
+ * infinities) saturate to the largest finite code, NaN gives 0x7F.  The code
+ * is found by searching the decoder's table, so encode and decode agree by
+ * construction.  Used to quantise an FP8 output with a per-tensor scale. */
+uint8_t oracle_e4m3_encode(double x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return sign | 0x7E;
+    int e2;
+    frexp(a, &e2);          /* a = f * 2^e2 with f in [0.5, 1): binade 2^(e2-1) */
+    int E = e2 - 1;
+    if (E < -6) E = -6;     /* subnormals share the smallest normal binade's spacing */
+    double q = ldexp(1.0, E - 3);
+    double v = rint(a / q) * q;  /* default rounding mode: nearest, ties to even */
+    for (int c = 0; c <= 0x7E; ++c)
+        if (oracle_e4m3_to_double((uint8_t)c) == v) return sign | (uint8_t)c;
+    return 0x7F;            /* unreachable: every rounded value is on the grid */
+}
+
+void oracle_e4m3_encode_array(const double* src, uint8_t* dst, int64_t n) {
+    for (int64_t k = 0; k < n; ++k) dst[k] = oracle_e4m3_encode(src[k]);
+}
+
 void oracle_bf16_array_to_double(const uint16_t* src, double* dst, int64_t n) {
     for (int64_t k = 0; k < n; ++k) dst[k] = oracle_bf16_to_double(src[k]);
 }

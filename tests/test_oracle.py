@@ -335,3 +335,53 @@ def test_range_rejects_ranges_outside_the_sequence():
         oracle.decode_range(inp, [0, 10], [6, 60])  # past L for request 0
     with pytest.raises(ValueError):
         oracle.decode_range(inp, [3, 10], [2, 60])  # hi < lo
+
+
+# ---------------------------------------------------------------------------
+# FP8 query and FP8 output (the TokenSpeed MLA summary: the decode takes FP8
+# scales, "output_scale" among them, in implementation breakdown 1, and its
+# review names the follow-up "Fix decode FP8 numerics: pass output_scale and
+# assert FP8 Q").  The query is E4M3 codes times one per-tensor q_scale; an FP8
+# output is the E4M3 code of out / out_scale (round to nearest even, saturating).
+
+def test_e4m3_encoder_matches_torch_rounding():
+    # A dense sweep over the whole finite range, with every grid point, every
+    # midpoint between neighbours (ties) and the float32 values on either side
+    # of it, in both signs.  The values are float32 (torch rounds a float64 to
+    # float32 first, and the kernel quantises float32 values), so both sides
+    # round each value once.
+    codes = torch.arange(0x7F, dtype=torch.int32).to(torch.uint8)
+    grid = codes.view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    mids = (grid[1:] + grid[:-1]) / 2
+    g = np.random.default_rng(0)
+    rand = np.concatenate([g.uniform(0, 464, 20000), np.exp(g.uniform(np.log(1e-4), np.log(464), 20000))])
+    xs = np.concatenate([grid, mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9)),
+                         rand.astype(np.float32), [np.float32(464.0)]]).astype(np.float32)
+    xs = np.concatenate([xs, -xs])
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_encode(xs.astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_e4m3_encoder_saturates_and_round_trips():
+    big = np.array([464.0000001, 480.0, 1e9, np.inf])
+    assert np.all(oracle.e4m3_encode(big) == 0x7E)
+    assert np.all(oracle.e4m3_encode(-big) == 0xFE)
+    assert oracle.e4m3_encode(np.array([np.nan]))[0] == 0x7F
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.e4m3_encode(oracle.e4m3_to_f64(finite)), finite)
+
+
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_fp8_query_matches_torch_sdpa_on_dequantised_values(q_len):
+    inp = small(seed=30 + q_len, q_len=q_len, kv_lens=(q_len, 70, 190), fp8=True, q_fp8=True, sharp=3.0)
+    assert inp.q_nope.dtype == torch.uint8 and inp.q_scale != 1.0
+    out, lse = oracle.decode(inp)
+    # torch's own float8 decode of the same codes, times the scale
+    deq = synth.Inputs(**{**inp.__dict__})
+    deq.q_nope = inp.q_nope.view(torch.float8_e4m3fn).to(torch.float64) * inp.q_scale
+    deq.q_pe = inp.q_pe.view(torch.float8_e4m3fn).to(torch.float64) * inp.q_scale
+    deq.q_fp8 = False
+    ref_o, ref_l = sdpa_reference(deq)
+    assert np.max(np.abs(out - ref_o)) <= 1e-12
+    assert np.max(np.abs(lse - ref_l)) <= 1e-12
