@@ -38,17 +38,23 @@ SPLIT_KERNEL_FILES = ("mla_split_kv_tc.cu", "ptx_sm100.cuh", "common.cuh")
 def algorithmic_bytes(inp, out_elem_bytes):
     """Every visible KV row read once, Q read once, out + lse written once."""
     e = 1 if inp.kv_fp8 else 2
+    qe = 1 if inp.q_fp8 else 2
     rows = inp.batch * inp.q_len * inp.num_heads
     kv = int(inp.seq_lens.to(torch.int64).sum().item()) * 576 * e
-    return kv + rows * 576 * 2 + rows * (512 * out_elem_bytes + 4)
+    return kv + rows * 576 * qe + rows * (512 * out_elem_bytes + 4)
+
+
+def visible_pairs(inp):
+    """(row, token) pairs the causal mask lets through: sum over requests, heads and
+    query rows i of L - q_len + 1 + i."""
+    L = inp.seq_lens.to(torch.int64)
+    q = inp.q_len
+    return int((q * L - q * (q - 1) // 2).sum().item()) * inp.num_heads
 
 
 def algorithmic_flops(inp):
     """2*576 (QK) + 2*512 (PV) flops per visible (row, token) pair."""
-    L = inp.seq_lens.to(torch.int64)
-    q = inp.q_len
-    pairs = int((q * L - q * (q - 1) // 2).sum().item()) * inp.num_heads
-    return 2176 * pairs
+    return 2176 * visible_pairs(inp)
 
 
 def read_peaks():
@@ -247,26 +253,42 @@ def main():
 
     _lib.load()
     name = args.workload
-    inp = synth.make_inputs(name, seed=rank_seed(list(synth.WORKLOADS).index(name), rank), device="cuda",
-                            batch=args.batch)
+    # "fp8q" is the FP8 workload with an FP8 query too (QK^T on the FP8 tensor
+    # path through mla_decode_fp8); its data are the FP8 workload's draws.
+    q8 = name == "fp8q"
+    base = "fp8" if q8 else name
+    inp = synth.make_inputs(base, seed=rank_seed(list(synth.WORKLOADS).index(base), rank), device="cuda",
+                            batch=args.batch, q_fp8=q8)
     pl = api.plan_for(inp, force_splits=args.force_splits)
     ws = api.alloc_workspace(pl, "cuda")
     out, lse = api.alloc_outputs(inp)
     kvs = api.kv_scale_tensor(inp)
+    qs = torch.tensor([inp.q_scale], dtype=torch.float32, device="cuda") if q8 else None
     stream = torch.cuda.current_stream()
     qn, qp = inp.q_nope.view(-1, 512), inp.q_pe.view(-1, 64)
 
-    def step(ev=None):
+    def call(qn_, qp_, bt_, sl_, ev=None):
+        """One decode; with events, [0]-[1] brackets the split kernel and [1]-[2] the
+        combine (an FP8-query call is one C call: [0]-[1] brackets both)."""
         if ev:
             ev[0].record(stream)
-        st = _lib.split_kv(pl, qn, qp, inp.kv_cache, inp.block_table, inp.seq_lens, inp.softmax_scale,
-                           kvs, out, lse, ws, stream)
-        if ev:
-            ev[1].record(stream)
-        st2 = _lib.combine(pl, out, lse, ws, stream)
+        if q8:
+            st = _lib.decode_fp8(pl, qn_, qp_, qs, inp.kv_cache, bt_, sl_, inp.softmax_scale, kvs, out, None, lse,
+                                 ws, stream)
+            st2 = 0
+            if ev:
+                ev[1].record(stream)
+        else:
+            st = _lib.split_kv(pl, qn_, qp_, inp.kv_cache, bt_, sl_, inp.softmax_scale, kvs, out, lse, ws, stream)
+            if ev:
+                ev[1].record(stream)
+            st2 = _lib.combine(pl, out, lse, ws, stream)
         if ev:
             ev[2].record(stream)
         assert st == 0 and st2 == 0, (st, st2)
+
+    def step(ev=None):
+        call(qn, qp, inp.block_table, inp.seq_lens, ev)
 
     for _ in range(args.warmup):
         step()
@@ -316,7 +338,11 @@ def main():
         d_qp.copy_(h_qp, non_blocking=True)
         d_bt.copy_(h_bt, non_blocking=True)
         d_sl.copy_(h_sl, non_blocking=True)
-        st = _lib.decode(pl, d_qn, d_qp, inp.kv_cache, d_bt, d_sl, inp.softmax_scale, kvs, out, lse, ws, stream)
+        if q8:
+            st = _lib.decode_fp8(pl, d_qn, d_qp, qs, inp.kv_cache, d_bt, d_sl, inp.softmax_scale, kvs, out, None,
+                                 lse, ws, stream)
+        else:
+            st = _lib.decode(pl, d_qn, d_qp, inp.kv_cache, d_bt, d_sl, inp.softmax_scale, kvs, out, lse, ws, stream)
         assert st == 0
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
@@ -347,7 +373,15 @@ def main():
     # HBM for few query rows per page, the tensor pipe for many (e.g. 256 rows).
     hbm = {"achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": achieved_gbs / hbm_peak}
     tc = {"achieved": achieved_tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved_tf / tc_peak}
-    if aflops / (tc_peak * 1e12) > abytes / (hbm_peak * 1e9):
+    if q8:
+        # QK^T (2*576 flops per pair) runs at the FP8 rate, taken as the measured
+        # bf16 peak x 2 (the nominal dense fp8/bf16 ratio); PV (2*512) at bf16.
+        pairs = visible_pairs(inp)
+        floor_s = 1152 * pairs / (2 * tc_peak * 1e12) + 1024 * pairs / (tc_peak * 1e12)
+        eff_peak = aflops / floor_s / 1e12
+        tc = {"achieved": achieved_tf, "peak": eff_peak, "unit": "TFLOP/s", "frac": achieved_tf / eff_peak,
+              "peak_note": "QK at 2x measured bf16 (fp8), PV at measured bf16; timed split+combine"}
+    if aflops / (tc["peak"] * 1e12) > abytes / (hbm_peak * 1e9):
         roofline = {"bound": "tensor", **tc, "traffic": traffic, "peak_source": peak_kind, "hbm": hbm}
     else:
         roofline = {"bound": "hbm", **hbm, "traffic": traffic, "peak_source": peak_kind, "tensor": tc}
@@ -355,17 +389,20 @@ def main():
     line = {
         "metric": METRIC, "value": step_us, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_us / 1e3, "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 KV, bf16 MMA, f32 accumulate" if inp.kv_fp8 else "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": ("fp8-e4m3 Q and KV (QK on the fp8 tensor path), bf16 PV, f32 accumulate" if q8 else
+                  "fp8-e4m3 KV, bf16 MMA, f32 accumulate" if inp.kv_fp8 else "bf16"),
         "data": "synthetic",
         "config": {"workload": f"{name}: B={inp.batch} H={inp.num_heads} q_len={inp.q_len} "
                                f"kv_len={'x'.join(sorted(set(str(int(x)) for x in inp.seq_lens.tolist()))) if len(set(inp.seq_lens.tolist())) == 1 else 'mixed'} "
-                               f"page=64 {'e4m3' if inp.kv_fp8 else 'bf16'} KV",
+                               f"page=64 {'e4m3' if inp.kv_fp8 else 'bf16'} KV"
+                               f"{', e4m3 Q' if q8 else ''}",
                    "num_kv_splits": pl.num_kv_splits, "chunk_tokens": pl.chunk_tokens,
                    "row_groups": pl.row_groups, "partial_bytes": pl.partial_bytes,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "gb_per_s": abytes * world / (step_us * 1e-6) / 1e9,
         "tflops": aflops * world / (step_us * 1e-6) / 1e12,
-        "kernel_us": {"split_kv": split_us, "combine": comb_us},
+        "kernel_us": ({"split_kv+combine": split_us} if q8 else {"split_kv": split_us, "combine": comb_us}),
         "roofline": roofline,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * (1 + (pl.num_kv_splits > 1)),

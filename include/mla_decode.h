@@ -49,7 +49,8 @@ typedef enum {
 } mla_status_t;
 
 typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype_t;
-typedef enum { MLA_OUT_BF16 = 0, MLA_OUT_FP32 = 1 } mla_out_dtype_t;
+/* MLA_OUT_FP8_E4M3 (e4m3 codes of out / out_scale) only through mla_decode_fp8. */
+typedef enum { MLA_OUT_BF16 = 0, MLA_OUT_FP32 = 1, MLA_OUT_FP8_E4M3 = 2 } mla_out_dtype_t;
 
 /* Fixed geometry of the latent cache (DeepSeek-R1). */
 #define MLA_KV_LORA_RANK 512
@@ -200,6 +201,37 @@ mla_status_t mla_decode_varlen(const mla_decode_plan_t* plan, const void* q_nope
                                float softmax_scale, const float* kv_scale, void* out,
                                mla_out_dtype_t out_dtype, float* lse, void* workspace,
                                size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * mla_decode_fp8 -- mla_decode with an FP8 query over an FP8 cache, and an
+ * optional FP8 output (the TokenSpeed MLA summary: the decode is handed FP8
+ * scales, output_scale among them, implementation breakdown 1; its review
+ * names the follow-up "pass output_scale and assert FP8 Q").  QK^T runs on
+ * the e4m3 codes of query and cache on the FP8 tensor path (products of e4m3
+ * codes are exact, so the scores equal those on the dequantised values up to
+ * fp32 summation order); P and V stay bf16 for PV, V being the cache codes
+ * widened exactly.
+ *
+ * Same arguments as mla_decode, except:
+ *   plan    : kv_dtype must be MLA_KV_FP8_E4M3 (else MLA_ERR_UNSUPPORTED)
+ *   q_nope, q_pe : e4m3 codes, rows (b,i,h), 512 and 64 used; row strides in
+ *             elements (= bytes), multiples of 16; bases 16-byte aligned
+ *   q_scale : device fp32, query = code * q_scale (one per-tensor scale for
+ *             q_nope and q_pe; NULL = 1.0); read on every launch
+ *   out_dtype : MLA_OUT_BF16, MLA_OUT_FP32 or MLA_OUT_FP8_E4M3
+ *   out_scale : device fp32 for MLA_OUT_FP8_E4M3 (NULL = 1.0): every output
+ *             element is the e4m3 code of out / out_scale, rounded to nearest
+ *             even and saturated to +-448 (NaN rows of a rejected request stay
+ *             NaN); ignored for the other output types
+ * lse stays fp32.
+ */
+mla_status_t mla_decode_fp8(const mla_decode_plan_t* plan, const void* q_nope, int64_t q_nope_row_stride,
+                            const void* q_pe, int64_t q_pe_row_stride, const float* q_scale,
+                            const void* kv_cache, int num_pages, const int32_t* block_table,
+                            int block_table_stride, const int32_t* seq_lens, float softmax_scale,
+                            const float* kv_scale, void* out, mla_out_dtype_t out_dtype,
+                            const float* out_scale, float* lse, void* workspace, size_t workspace_bytes,
+                            void* cuda_stream);
 
 /*
  * mla_decode_shard -- one rank's part of a decode whose cache is sharded by

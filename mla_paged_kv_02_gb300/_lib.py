@@ -27,6 +27,7 @@ MLA_KV_BF16 = 0
 MLA_KV_FP8_E4M3 = 1
 MLA_OUT_BF16 = 0
 MLA_OUT_FP32 = 1
+MLA_OUT_FP8_E4M3 = 2
 
 # Every symbol include/mla_decode.h declares.
 EXPORTED = (
@@ -38,6 +39,7 @@ EXPORTED = (
     "mla_decode_check_error",
     "mla_decode_noalloc",
     "mla_decode_varlen",
+    "mla_decode_fp8",
     "mla_decode_shard",
     "mla_combine_shards",
     "mla_status_string",
@@ -73,17 +75,35 @@ class MlaError(RuntimeError):
 
 
 _lib = None
+_debug_lib = None
+DEBUG_LIB_PATH = os.path.join(_HERE, "libmla_decode_debug.so")
 
 
 def load() -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
+    _lib = _open(LIB_PATH)
+    return _lib
+
+
+def load_debug() -> ctypes.CDLL:
+    """The debug build (same kernels, plus mla_debug_set_wait_limit_ns); tests only."""
+    global _debug_lib
+    if _debug_lib is None:
+        lib = _open(DEBUG_LIB_PATH)
+        lib.mla_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.mla_debug_set_wait_limit_ns.restype = ctypes.c_int
+        _debug_lib = lib
+    return _debug_lib
+
+
+def _open(path: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
         raise RuntimeError(
-            f"CUDA library {LIB_PATH} is missing; build it with "
+            f"CUDA library {path} is missing; build it with "
             "`python -c 'import __graft_entry__ as g; g.build()'`")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(path)
     P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     PP = ctypes.POINTER(Plan)
     lib.mla_decode_plan.argtypes = [I, I, I, I, I, I, I, I, PP]
@@ -95,6 +115,7 @@ def load() -> ctypes.CDLL:
     lib.mla_decode_check_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.mla_decode_noalloc.argtypes = [PP, P, I64, P, I64, P, I, P, I, P, F, P, P, I, P, P]
     lib.mla_decode_varlen.argtypes = [PP, P, I64, P, I64, P, I, P, I, P, P, F, P, P, I, P, P, SZ, P]
+    lib.mla_decode_fp8.argtypes = [PP, P, I64, P, I64, P, P, I, P, I, P, F, P, P, I, P, P, P, SZ, P]
     lib.mla_decode_shard.argtypes = [PP, P, I64, P, I64, P, I, P, I, P, P, P, F, P, P, P, SZ, P]
     lib.mla_combine_shards.argtypes = [I64, I, P, P, I, P, P]
     lib.mla_status_string.argtypes = [I]
@@ -102,7 +123,6 @@ def load() -> ctypes.CDLL:
     for name in EXPORTED:
         if name != "mla_status_string":
             getattr(lib, name).restype = I
-    _lib = lib
     return lib
 
 
@@ -207,3 +227,22 @@ def combine_shards(shard_partials, out, lse, stream=None) -> int:
     return load().mla_combine_shards(rows, R, _ptr(shard_partials), _ptr(out),
                                      MLA_OUT_FP32 if out.dtype == torch.float32 else MLA_OUT_BF16, _ptr(lse),
                                      _stream(stream))
+
+
+def out_dtype_code(out: torch.Tensor) -> int:
+    if out.dtype == torch.float32:
+        return MLA_OUT_FP32
+    if out.dtype == torch.uint8:
+        return MLA_OUT_FP8_E4M3
+    return MLA_OUT_BF16
+
+
+def decode_fp8(pl: Plan, q_nope, q_pe, q_scale, kv_cache, block_table, seq_lens, softmax_scale, kv_scale, out,
+               out_scale, lse, workspace, stream=None) -> int:
+    """mla_decode_fp8: e4m3 query codes (uint8) with a device q_scale; ``out`` as
+    uint8 selects an FP8 output (codes of out / out_scale)."""
+    return load().mla_decode_fp8(
+        ctypes.byref(pl), _ptr(q_nope), q_nope.stride(-2), _ptr(q_pe), q_pe.stride(-2), _ptr(q_scale),
+        _ptr(kv_cache), kv_cache.shape[0], _ptr(block_table), block_table.stride(0), _ptr(seq_lens),
+        float(softmax_scale), _ptr(kv_scale), _ptr(out), out_dtype_code(out), _ptr(out_scale), _ptr(lse),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,10 +22,12 @@ constexpr int kPartRow = kKvLora + 1;      // one split partial: 512 outputs + L
 constexpr int kHdrCode = 0, kHdrRequest = 1, kHdrIndex = 2, kHdrValue = 3;
 
 struct DecodeParams {
-  const __nv_bfloat16* q_nope;
+  const void* q_nope;     // bf16, or e4m3 codes when q_fp8
   int64_t q_nope_stride;  // elements between consecutive (b,i,h) rows
-  const __nv_bfloat16* q_pe;
+  const void* q_pe;
   int64_t q_pe_stride;
+  int q_fp8;              // the query is e4m3 codes times *q_scale (FP8 cache only)
+  const float* q_scale;   // device scalar or nullptr (1)
   const void* kv;  // [num_pages, 64, 576] bf16 or e4m3 bytes
   int num_pages;
   int kv_fp8;
@@ -39,8 +42,10 @@ struct DecodeParams {
   const int32_t* total_lens;
   float softmax_scale;
   const float* kv_scale;  // device scalar or nullptr
-  void* out;              // [B*R rows] of 512 bf16 or fp32, out_stride elements apart
+  void* out;              // [B*R rows] of 512 bf16, fp32 or e4m3, out_stride elements apart
   int out_fp32;
+  int out_fp8;            // e4m3 code of out / *out_scale (round to nearest even, saturating)
+  const float* out_scale; // device scalar or nullptr (1)
   int64_t out_stride;     // 512, or 513 when out/lse are the two parts of a 513-wide partial row
   float* lse;       // [B*R] lse_stride apart, or nullptr
   int64_t lse_stride;
@@ -53,6 +58,9 @@ struct DecodeParams {
   int batch, num_heads, q_len, rows;  // rows = num_heads * q_len per request
   int max_seq_len, splits, chunk_tokens, rows_per_cta, row_groups;
   int order_by_length;  // clusters take the requests longest first (see kMaxOrderedBatch)
+  // Limit of every bounded device wait in ns (0: the built-in 1 s).  Only a
+  // library built with MLA_DEBUG lets a caller set it (to test the timeout path).
+  uint64_t wait_limit_ns;
 };
 
 // Batches up to this size are ranked by length inside the split kernel.
@@ -69,9 +77,17 @@ __device__ __forceinline__ void report_error(int32_t* err, int code, int request
   }
 }
 
-__device__ __forceinline__ void store_out(const DecodeParams& p, int64_t row, int d, float v) {
+// out / out_scale as an e4m3 code: round to nearest even, saturating to +-448;
+// NaN stays NaN (0x7F / 0xFF).
+__device__ __forceinline__ uint8_t to_e4m3(float v, float out_scale) {
+  return (uint8_t)__nv_cvt_float_to_fp8(v / out_scale, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ void store_out(const DecodeParams& p, int64_t row, int d, float v, float out_scale) {
   if (p.out_fp32)
     reinterpret_cast<float*>(p.out)[row * p.out_stride + d] = v;
+  else if (p.out_fp8)
+    reinterpret_cast<uint8_t*>(p.out)[row * p.out_stride + d] = to_e4m3(v, out_scale);
   else
     reinterpret_cast<__nv_bfloat16*>(p.out)[row * p.out_stride + d] = __float2bfloat16_rn(v);
 }

@@ -5,6 +5,9 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#ifdef MLA_DEBUG
+#include "mla_decode_debug.h"
+#endif
 
 using namespace mla;
 
@@ -51,6 +54,10 @@ bool plan_ok(const mla_decode_plan_t* pl) {
   return pl->partial_bytes == part && pl->workspace_bytes == MLA_WORKSPACE_HEADER_BYTES + part;
 }
 
+#ifdef MLA_DEBUG
+uint64_t g_debug_wait_limit_ns = 0;  // 0: the kernels' built-in limit
+#endif
+
 }  // namespace
 
 bool mla::plan_valid(const mla_decode_plan_t* pl) { return plan_ok(pl); }
@@ -59,30 +66,37 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// q_fp8: the query is e4m3 codes (1 byte each), which also admits an FP8
+// output; otherwise it is bf16 and the output bf16 or fp32.
 mla_status_t fill_params(const mla_decode_plan_t* pl, const void* q_nope, int64_t q_nope_row_stride,
                          const void* q_pe, int64_t q_pe_row_stride, const void* kv_cache,
                          int num_pages, const int32_t* block_table, int block_table_stride,
                          const int32_t* seq_lens, float softmax_scale, const float* kv_scale,
                          void* out, mla_out_dtype_t out_dtype, float* lse, void* workspace,
-                         size_t workspace_bytes, DecodeParams* p) {
+                         size_t workspace_bytes, DecodeParams* p, bool q_fp8 = false) {
   if (!plan_ok(pl)) return MLA_ERR_INVALID_ARG;
   if (!q_nope || !q_pe || !kv_cache || !block_table || !seq_lens || !out || !workspace)
     return MLA_ERR_INVALID_ARG;
+  // Row strides: whole rows, and 16-byte multiples (the TMA stride rule).
+  const int64_t stride_mult = q_fp8 ? 16 : 8;
   if (q_nope_row_stride < MLA_KV_LORA_RANK || q_pe_row_stride < MLA_QK_ROPE_DIM ||
-      q_nope_row_stride % 8 || q_pe_row_stride % 8)
+      q_nope_row_stride % stride_mult || q_pe_row_stride % stride_mult)
     return MLA_ERR_INVALID_ARG;
   if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(workspace, 256))
     return MLA_ERR_INVALID_ARG;
   if (num_pages < 1 || (int64_t)num_pages * MLA_PAGE_SIZE > INT32_MAX) return MLA_ERR_INVALID_ARG;
   if (block_table_stride < ceil_div(pl->max_seq_len, MLA_PAGE_SIZE)) return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
-  if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_FP32) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_FP32 && !(q_fp8 && out_dtype == MLA_OUT_FP8_E4M3))
+    return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < pl->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
 
   memset(p, 0, sizeof *p);
-  p->q_nope = static_cast<const __nv_bfloat16*>(q_nope);
+  p->q_fp8 = q_fp8;
+  p->out_fp8 = out_dtype == MLA_OUT_FP8_E4M3;
+  p->q_nope = q_nope;
   p->q_nope_stride = q_nope_row_stride;
-  p->q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+  p->q_pe = q_pe;
   p->q_pe_stride = q_pe_row_stride;
   p->kv = kv_cache;
   p->num_pages = num_pages;
@@ -112,6 +126,9 @@ mla_status_t fill_params(const mla_decode_plan_t* pl, const void* q_nope, int64_
   // to start (with a single wave the order does not matter).
   const int64_t clusters = (int64_t)pl->batch * pl->row_groups * pl->num_kv_splits;
   p->order_by_length = pl->batch <= kMaxOrderedBatch && clusters > pl->num_sms / 2;
+#ifdef MLA_DEBUG
+  p->wait_limit_ns = g_debug_wait_limit_ns;
+#endif
   return MLA_OK;
 }
 
@@ -220,15 +237,19 @@ namespace {
 // lse (stride lse_stride).
 mla_status_t combine_workspace(const mla_decode_plan_t* plan, void* out, mla_out_dtype_t out_dtype,
                                int64_t out_stride, float* lse, int64_t lse_stride, const void* workspace,
-                               size_t workspace_bytes, void* cuda_stream) {
+                               size_t workspace_bytes, void* cuda_stream, const float* out_scale = nullptr) {
   if (!plan_ok(plan) || !out || !workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
-  if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_FP32) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_FP32 &&
+      !(out_dtype == MLA_OUT_FP8_E4M3 && out_stride == MLA_KV_LORA_RANK))
+    return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
   if (plan->num_kv_splits == 1) return MLA_OK;
   DecodeParams p;
   memset(&p, 0, sizeof p);
   p.out = out;
   p.out_fp32 = out_dtype == MLA_OUT_FP32;
+  p.out_fp8 = out_dtype == MLA_OUT_FP8_E4M3;
+  p.out_scale = out_scale;
   p.out_stride = out_stride;
   p.lse = lse;
   p.lse_stride = lse_stride;
@@ -278,6 +299,25 @@ mla_status_t mla_decode_shard(const mla_decode_plan_t* plan, const void* q_nope,
   if (launch_split_kv(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
   return combine_workspace(plan, shard_partial, MLA_OUT_FP32, kPartRow, shard_partial + MLA_KV_LORA_RANK,
                            kPartRow, workspace, workspace_bytes, cuda_stream);
+}
+
+mla_status_t mla_decode_fp8(const mla_decode_plan_t* plan, const void* q_nope, int64_t q_nope_row_stride,
+                            const void* q_pe, int64_t q_pe_row_stride, const float* q_scale, const void* kv_cache,
+                            int num_pages, const int32_t* block_table, int block_table_stride,
+                            const int32_t* seq_lens, float softmax_scale, const float* kv_scale, void* out,
+                            mla_out_dtype_t out_dtype, const float* out_scale, float* lse, void* workspace,
+                            size_t workspace_bytes, void* cuda_stream) {
+  if (plan && plan->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
+  DecodeParams p;
+  mla_status_t st = fill_params(plan, q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache, num_pages,
+                                block_table, block_table_stride, seq_lens, softmax_scale, kv_scale, out, out_dtype,
+                                lse, workspace, workspace_bytes, &p, /*q_fp8=*/true);
+  if (st != MLA_OK) return st;
+  p.q_scale = q_scale;
+  p.out_scale = out_scale;
+  if (launch_split_kv(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return combine_workspace(plan, out, out_dtype, MLA_KV_LORA_RANK, lse, 1, workspace, workspace_bytes, cuda_stream,
+                           out_scale);
 }
 
 mla_status_t mla_combine_shards(int64_t rows, int num_shards, const float* shard_partials, void* out,
@@ -353,6 +393,13 @@ mla_status_t mla_decode_check_error(void* workspace, void* cuda_stream, int32_t 
   }
   return MLA_OK;
 }
+
+#ifdef MLA_DEBUG
+mla_status_t mla_debug_set_wait_limit_ns(uint64_t ns) {
+  g_debug_wait_limit_ns = ns;
+  return MLA_OK;
+}
+#endif
 
 const char* mla_status_string(mla_status_t status) {
   switch (status) {

@@ -73,8 +73,9 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams
 #pragma unroll
     for (int k = 0; k < 16; ++k) o[k] = NAN;
   }
+  const float osc = (p.out_fp8 && p.out_scale) ? *p.out_scale : 1.f;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) store_out(p, row, lane + 32 * k, o[k]);
+  for (int k = 0; k < 16; ++k) store_out(p, row, lane + 32 * k, o[k], osc);
   if (p.lse && lane == 0) p.lse[row * p.lse_stride] = lse;
 }
 

@@ -100,6 +100,20 @@ struct Layout {
   static_assert(kStageBytes % 1024 == 0 && kPOff % 1024 == 0 && kQpeOff % 1024 == 0, "swizzle atoms");
 };
 
+// FP8 query (kQ8, FP8 cache): QK^T runs on the e4m3 codes themselves
+// (tcgen05 kind::f8f6f4).  The CTA's 256 e4m3 c_kv columns of a page land
+// 128B-swizzled as two 8 KB boxes at stage + 16 KB, the space of bf16 V chunks 2
+// and 3, which the converter writes only once QK of the page has completed; its
+// 32 e4m3 k_pe columns land 32B-swizzled at stage + 32 KB and are never
+// overwritten (k_pe needs no bf16 copy: it only enters QK).  The query's c_kv
+// columns sit in tensor memory four codes per column, its 32 q_pe codes per row
+// in shared memory (32B swizzle).
+constexpr int kQ8RawOff = 16 * 1024;
+constexpr int kQ8RawPeOff = 32 * 1024;
+constexpr int kQ8Box = 64 * 128;     // 64 tokens x 128 e4m3 columns
+constexpr int kQ8PeBox = 64 * 32;    // 64 tokens x 32 e4m3 k_pe columns
+constexpr int kQ8QpeBytes = 128 * 32;
+
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // O_c: 256 columns
 constexpr uint32_t kColS = 256;  // S: two 64-column buffers
@@ -118,8 +132,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s: far above any legitimate wait
+// After an abort a CTA lingers this long before the final cluster barrier, so
+// that bulk copies and st.async stores it or its peer issued before giving up
+// (a few KB each, microseconds in flight) have landed before either CTA exits.
+constexpr uint64_t kAbortSettleNs = 200000ull;
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
+constexpr uint32_t kIdescQK8 = idesc_e4m3(128, 64);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
 
 // Bytes the peer's warp of a quadrant delivers per page: its 32 rows' P halves
@@ -143,6 +162,7 @@ struct Ctl {
   uint64_t u_ready[2];         // the peer's references for the page landed (count 4 + 512 B)
   uint64_t checked[2];         // the 4 local warps ran the page's reference check (count 4)
   uint64_t p_recv[4];          // per quadrant: the peer holds this CTA's P rows it had to scale (count 1, remote)
+  uint64_t qk_done[kMaxStages];  // FP8 query: QK^T of the stage's page completed (its e4m3 bytes are free)
   uint64_t fin;                // the peer's row sums delivered (count 4 + 512 B)
   uint64_t drain;
   uint32_t tmem_base;
@@ -207,12 +227,13 @@ __device__ __forceinline__ bool wait_bar(Ctl* c, uint64_t* bar, uint32_t parity,
   auto test = [&]() { return kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
   if (test()) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
   while (true) {
 #pragma unroll 1
     for (int k = 0; k < 32; ++k)
       if (test()) return true;
     if (*(volatile int*)&c->abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit) {
       *(volatile int*)&c->abort = 1;
       report_error(p.err, MLA_ERR_TIMEOUT, c->req, where, blockIdx.y);
       return false;
@@ -220,11 +241,12 @@ __device__ __forceinline__ bool wait_bar(Ctl* c, uint64_t* bar, uint32_t parity,
   }
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kQ8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(), 1)
     split_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
                        const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kv3,
                        const __grid_constant__ CUtensorMap tm_kpe, const DecodeParams p) {
+  static_assert(kFp8 || !kQ8, "an FP8 query needs the FP8 cache");
   using Lay = Layout<kFp8>;
   constexpr int kStageBytes = Lay::kStageBytes;
   constexpr int kNS = Lay::kStages;
@@ -259,6 +281,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       mbar_init(&ctl->raw_full[s], 1);
       mbar_init(&ctl->full[s], kFp8 ? 4 : 1);
       mbar_init(&ctl->empty[s], 1);
+      mbar_init(&ctl->qk_done[s], 1);
     }
     mbar_init(&ctl->q_tmem, 4);
     mbar_init(&ctl->s_full[0], 1);
@@ -339,6 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   const int n_pages = hi > lo ? (hi + kPage - 1) / kPage - first_page : 0;
   const int row0 = rg * kRows;
   const float kv_scale = (kFp8 && p.kv_scale) ? *p.kv_scale : 1.0f;
+  const float q_scale = (kQ8 && p.q_scale) ? *p.q_scale : 1.0f;  // folded into the softmax scale
   const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride + first_page;
 
   // Thread 0 is the TMA producer: it starts Q's loads (into this CTA's own
@@ -356,8 +380,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       prefetch_tmap(&tm_qn);
       prefetch_tmap(&tm_qp);
       const int qrow = b * p.rows + row0;
-      mbar_arrive_expect_tx(&ctl->q_full, 4 * kQChunkBytes + kQChunkBytes / 2);
-      for (int k = 0; k < 4; ++k) tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, (g0 + k) * 64, qrow);
+      if (kQ8) {  // two 128-code boxes of the CTA's c_kv columns, and its 32 q_pe codes
+        mbar_arrive_expect_tx(&ctl->q_full, 2 * kQChunkBytes + kQ8QpeBytes);
+        for (int k = 0; k < 2; ++k)
+          tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, 256 * (int)cta + 128 * k, qrow);
+      } else {
+        mbar_arrive_expect_tx(&ctl->q_full, 4 * kQChunkBytes + kQChunkBytes / 2);
+        for (int k = 0; k < 4; ++k) tma_load_2d(sQ + k * kQChunkBytes, &tm_qn, &ctl->q_full, (g0 + k) * 64, qrow);
+      }
       tma_load_2d(sQpe, &tm_qp, &ctl->q_full, 32 * (int)cta, qrow);
       prefetch_tmap(&tm_kv);
       if (!kFp8) prefetch_tmap(&tm_kv3);
@@ -387,6 +417,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         if (page < 0 || page >= p.num_pages) {
           if (cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, first_page + j, page);
           mbar_arrive(land);  // nothing to load; consumers mask the whole page
+        } else if (kQ8) {  // e4m3 for QK^T as it is: two 128B-swizzled c_kv boxes, one k_pe box
+          mbar_arrive_expect_tx(land, 2 * kQ8Box + kQ8PeBox);
+          for (int k = 0; k < 2; ++k)
+            tma_load_2d(stage + kQ8RawOff + k * kQ8Box, &tm_kv, land, 256 * (int)cta + 128 * k, page * kPage);
+          tma_load_2d(stage + kQ8RawPeOff, &tm_kpe, land, 8 * 64 + 32 * (int)cta, page * kPage);
         } else if (kFp8) {  // e4m3: the CTA's four c_kv chunks and 32 k_pe columns
           mbar_arrive_expect_tx(land, 4 * kRawBox + kRawPeBox);
           for (int k = 0; k < 4; ++k)
@@ -416,7 +451,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // thread of its own (below), so a PV that becomes ready never waits behind
     // the issue of a QK; the stage ring, S, S_in and P barriers bound how far QK
     // runs ahead.
-    if (lane == 0 && n_pages > 0) {
+    if (lane == 0 && n_pages > 0 && kQ8) {
+      // FP8 query: QK(j) on the page's e4m3 codes as soon as they land (the
+      // converter's bf16 V is only needed by PV): 8 K-steps of 32 codes over the
+      // two c_kv boxes, A from tensor memory, and one over the 32 k_pe codes, A
+      // (q_pe) from shared memory.  qk_done tells the converter that the codes
+      // under V chunks 2 and 3 may be overwritten.
+      const uint32_t kv_addr = smem_u32(sKV);
+      const uint64_t qpe_desc = sdesc_sw32(smem_u32(sQpe), 16, 256);
+      bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
+      for (int j = 0; ok && j < n_pages; ++j) {
+        const int st = j % kNS;
+        if (!wait_bar(ctl, &ctl->raw_full[st], (j / kNS) & 1, p, 3) ||
+            !wait_bar(ctl, &ctl->s_free[j & 1], ((j >> 1) & 1) ^ 1, p, 4))
+          break;
+        tc_fence_after();
+        const uint32_t stage = kv_addr + st * kStageBytes;
+        const uint32_t d = tmem + kColS + (j & 1) * 64;
+        for (int k = 0; k < 2; ++k) {
+          const uint64_t k_desc = sdesc_sw128(stage + kQ8RawOff + k * kQ8Box, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // 32 codes per K-step: 32 bytes of the swizzled row, 8 TMEM columns
+            mma_f8_ts(d, tmem + kColQ + k * 32 + kk * 8, k_desc + (uint64_t)((kk * 32) >> 4), kIdescQK8,
+                      (k | kk) ? 1u : 0u);
+        }
+        mma_f8_ss(d, qpe_desc, sdesc_sw32(stage + kQ8RawPeOff, 16, 256), kIdescQK8, 1u);
+        mma_commit(&ctl->s_full[j & 1]);
+        mma_commit(&ctl->qk_done[st]);
+      }
+      mma_commit(&ctl->drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(smem_u32(&ctl->drain), 0))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    } else if (lane == 0 && n_pages > 0) {
       const uint32_t kv_addr = smem_u32(sKV);
       const uint64_t qpe_desc = sdesc_sw64(smem_u32(sQpe), 16, 512);
       bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
@@ -458,6 +525,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       bool ok = true;
       for (int j = 0; ok && j < n_pages; ++j) {
         if (!wait_bar(ctl, &ctl->checked[j & 1], (j >> 1) & 1, p, 7)) break;
+        // With an FP8 query QK(j) did not wait for the converter: V must be in.
+        if (kQ8 && !wait_bar(ctl, &ctl->full[j % kNS], (j / kNS) & 1, p, 24)) break;
         tc_fence_after();
         const int pb = j % Lay::kPBufs;
         const uint64_t v_desc = sdesc_sw128(kv_addr + (j % kNS) * kStageBytes, kKvChunkBytes, 1024);
@@ -487,6 +556,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(smem_u32(&ctl->drain), 0))
         if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  } else if (kQ8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
+    // ------------------------------------------------------------ e4m3 -> bf16 V (FP8 query)
+    // Thread ct converts token ct/2 of c_kv box ct%2 (128 codes, 128B-swizzled)
+    // into bf16 V chunks 2(ct%2) and 2(ct%2)+1, writing zeros for tokens at or
+    // past L and for a page that was never loaded (such slots may hold
+    // anything).  Box 1's bf16 output covers the codes QK reads, so it is
+    // written only once QK of the page has completed.
+    const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
+    const int t = ct >> 1, h = ct & 1;
+    int page_next = n_pages > 0 ? bt_row[0] : 0;
+    for (int j = 0; j < n_pages; ++j) {
+      const int st = j % kNS;
+      const int page = page_next;
+      if (j + 1 < n_pages) page_next = bt_row[j + 1];
+      const bool page_ok = page >= 0 && page < p.num_pages;
+      const bool zero = t >= (page_ok ? min(L - (lo + j * kPage), kPage) : 0);
+      if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[st], (j / kNS) & 1, p, 9))) break;
+      uint8_t* stage = sKV + st * kStageBytes;
+      uint4 raw[8];
+      const uint8_t* src = stage + kQ8RawOff + h * kQ8Box + t * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) raw[u] = *reinterpret_cast<const uint4*>(src + ((u ^ (t & 7)) << 4));
+      // Logical 16-code piece u of the row: bf16 chunk 2h + u/4, 16-byte units
+      // 2(u%4) and 2(u%4)+1 of token row t (128B swizzle).
+      auto write = [&]() {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint8_t* dst = stage + (2 * h + (u >> 2)) * kKvChunkBytes + t * 128;
+          const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+          uint32_t o[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            o[2 * q] = zero ? 0u : e4m3x2_to_bf16x2((uint16_t)(w[q] & 0xFFFFu));
+            o[2 * q + 1] = zero ? 0u : e4m3x2_to_bf16x2((uint16_t)(w[q] >> 16));
+          }
+          const int c0 = 2 * (u & 3);
+          *reinterpret_cast<uint4*>(dst + ((c0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+      };
+      conv_sync();  // every thread holds its codes before box 1's space is rewritten
+      if (h == 0) write();
+      if (conv_sync_or(!wait_bar(ctl, &ctl->qk_done[st], (j / kNS) & 1, p, 25))) break;
+      if (h == 1) write();
+      fence_proxy_async_smem();
+      conv_sync();
+      if (lane == 0) mbar_arrive(&ctl->full[st]);
     }
   } else if (kFp8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
     // ------------------------------------------------------------ e4m3 -> bf16 converter
@@ -611,7 +728,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     const int qi = (row0 + r) / p.num_heads;
     const bool row_live = row_ok && qi < qlb;  // not padding of a per-request q_len
     const int vis = Ltot - qlb + 1 + qi - kv0;  // tokens of this cache the row may see
-    const float sc2 = p.softmax_scale * kv_scale * kLog2e;
+    const float sc2 = p.softmax_scale * kv_scale * q_scale * kLog2e;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t col_own = kColS + 32 * cta;    // S columns of this CTA's token half (within a buffer)
     uint8_t* sin_row = sSin + quad * kSinQuadBytes + lane * 128;  // 32 fp32 of the peer's partial
@@ -735,7 +852,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->q_full, 0, p, 18))) {
         ok = false;
       } else {
-        for (int k = 0; k < 4; ++k) {
+        // bf16: four 64-column chunks (2 per TMEM column); FP8: two 128-code
+        // chunks (4 per column).  Either way a chunk row is 128 bytes.
+        for (int k = 0; k < (kQ8 ? 2 : 4); ++k) {
           const uint8_t* qrow = sQ + k * kQChunkBytes + r * 128;
           uint32_t w[2][16];
 #pragma unroll
@@ -837,7 +956,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       // hold anything, NaN included; zero this CTA's 256 V columns of them.
       // Thread t of the group clears half of token row t/2.
       const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
-      if (n_valid < kPage) {
+      if (!kQ8 && n_valid < kPage) {  // (with an FP8 query the converter writes those rows as zeros)
         const int t = r >> 1;
         if (t >= n_valid) {
           uint8_t* stage = sKV + (j % kNS) * kStageBytes;
@@ -1001,6 +1120,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr)
           if (rr < nr) dst[rr * p.out_stride] = col[rr];
+      } else if (p.out_fp8) {
+        const float osc = p.out_scale ? *p.out_scale : 1.f;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) + (grow0 + quad * 32) * p.out_stride + dim;
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr)
+          if (rr < nr) dst[rr * p.out_stride] = to_e4m3(col[rr], osc);
       } else {
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (grow0 + quad * 32) * p.out_stride + dim;
 #pragma unroll
@@ -1009,6 +1134,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       }
     }
     tc_fence_before();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && *(volatile int*)&ctl->abort) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kAbortSettleNs) {
+    }
   }
   __syncthreads();
   cluster_sync_all();  // no remote store or arrive can target a CTA that has exited
@@ -1064,9 +1195,41 @@ bool encode_kv_chunks(CUtensorMap* m, const void* base, uint64_t rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <bool kFp8, bool kQ8>
+cudaError_t launch_kernel(const dim3& grid, const CUtensorMap& tm_qn, const CUtensorMap& tm_qp,
+                          const CUtensorMap& tm_kv, const CUtensorMap& tm_kv3, const CUtensorMap& tm_kpe,
+                          const DecodeParams& p, cudaStream_t stream) {
+  auto kern = split_kv_tc_kernel<kFp8, kQ8>;
+  constexpr int kSmem = Layout<kFp8>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, block_threads<kFp8>(), kSmem, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, tm_kpe, p);
+  return cudaGetLastError();
+}
+
+// FP8 query: tensor maps over e4m3 codes, boxes shaped for QK^T on the codes
+// (128B swizzle for c_kv, 32B swizzle for the 32 rope codes of each CTA).
+cudaError_t launch_split_kv_q8(const DecodeParams& p, cudaStream_t stream) {
+  CUtensorMap tm_qn, tm_qp, tm_kv, tm_kpe;
+  const uint64_t q_rows = (uint64_t)p.batch * p.rows;
+  const uint64_t kv_rows = (uint64_t)p.num_pages * kPage;
+  if (!encode_2d(&tm_qn, p.q_nope, kKvLora, q_rows, p.q_nope_stride, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B, 128) ||
+      !encode_2d(&tm_qp, p.q_pe, kRope, q_rows, p.q_pe_stride, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 128,
+                 CU_TENSOR_MAP_SWIZZLE_32B, 32) ||
+      !encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                 128) ||
+      !encode_2d(&tm_kpe, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64, CU_TENSOR_MAP_SWIZZLE_32B,
+                 32))
+    return cudaErrorInvalidValue;
+  const dim3 grid(2 * p.row_groups, p.splits, p.batch);
+  return launch_kernel<true, true>(grid, tm_qn, tm_qp, tm_kv, tm_kv, tm_kpe, p, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
+  if (p.q_fp8) return p.kv_fp8 ? launch_split_kv_q8(p, stream) : cudaErrorInvalidValue;
   CUtensorMap tm_qn, tm_qp, tm_kv, tm_kv3, tm_kpe;
   const uint64_t q_rows = (uint64_t)p.batch * p.rows;
   const uint64_t kv_rows = (uint64_t)p.num_pages * kPage;
@@ -1090,20 +1253,8 @@ cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   if (p.kv_fp8) tm_kv3 = tm_kv;  // unused on the FP8 path
   const dim3 grid(2 * p.row_groups, p.splits, p.batch);
-  if (p.kv_fp8) {
-    auto kern = split_kv_tc_kernel<true>;
-    constexpr int kSmem = Layout<true>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, block_threads<true>(), kSmem, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, tm_kpe, p);
-  } else {
-    auto kern = split_kv_tc_kernel<false>;
-    constexpr int kSmem = Layout<false>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, block_threads<false>(), kSmem, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, tm_kpe, p);
-  }
-  return cudaGetLastError();
+  if (p.kv_fp8) return launch_kernel<true, false>(grid, tm_qn, tm_qp, tm_kv, tm_kv3, tm_kpe, p, stream);
+  return launch_kernel<false, false>(grid, tm_qn, tm_qp, tm_kv, tm_kv3, tm_kpe, p, stream);
 }
 
 }  // namespace mla

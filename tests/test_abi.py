@@ -22,10 +22,12 @@ def lib():
     return _lib.load()
 
 
-def declared_symbols():
+def declared_symbols(debug=False):
+    """Entry points declared by the product headers (or, with debug, by the debug
+    build's own header)."""
     names = set()
     for f in os.listdir(os.path.join(ROOT, "include")):
-        if f.endswith(".h"):
+        if f.endswith(".h") and f.endswith("_debug.h") == debug:
             text = open(os.path.join(ROOT, "include", f)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
             names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(mla_\w+)\s*\(", text, flags=re.M))
@@ -37,6 +39,16 @@ def test_exports_every_declared_symbol(lib):
     assert names == set(_lib.EXPORTED), names
     for n in names:
         assert hasattr(lib, n)
+
+
+def test_debug_build_exports_its_hook_and_every_product_symbol(lib):
+    dbg = _lib.load_debug()
+    hooks = declared_symbols(debug=True)
+    assert hooks == {"mla_debug_set_wait_limit_ns"}
+    for n in hooks | set(_lib.EXPORTED):
+        assert hasattr(dbg, n)
+    assert not hasattr(lib, "mla_debug_set_wait_limit_ns")  # the product build has no test hook
+    assert dbg.mla_debug_set_wait_limit_ns(0) == _lib.MLA_OK
 
 
 def test_status_strings(lib):
@@ -174,3 +186,23 @@ def test_decode_varlen_validation_rejects_before_launch(lib):
 
     assert call(q_lens=0) == E
     assert call(q_nope=0) == E
+
+
+def test_fp8_entry_point_validation(lib):
+    # mla_decode_fp8: an FP8 query needs an FP8 cache plan; query row strides
+    # are 16-byte multiples (e4m3: 16 elements); an FP8 output is accepted only
+    # here, not by mla_decode.
+    P = ctypes.c_void_p
+    pl8 = _lib.plan(2, 16, 1, 200, kv_fp8=True, num_sms=148, force_splits=2)
+    plb = _lib.plan(2, 16, 1, 200, num_sms=148, force_splits=2)
+
+    def call(pl, qs=512, ps=64, odt=_lib.MLA_OUT_FP8_E4M3):
+        return lib.mla_decode_fp8(ctypes.byref(pl), P(0x10000), qs, P(0x20000), ps, None, P(0x30000), 8,
+                                  P(0x40000), 4, P(0x50000), 0.07, None, P(0x60000), odt, None, None,
+                                  P(0x70000), pl.workspace_bytes, None)
+
+    assert call(plb) == _lib.MLA_ERR_UNSUPPORTED
+    assert call(pl8, qs=520) == _lib.MLA_ERR_INVALID_ARG  # 520 bytes: not a 16-byte multiple
+    assert call(pl8, ps=72) == _lib.MLA_ERR_INVALID_ARG
+    assert call(pl8, odt=7) == _lib.MLA_ERR_INVALID_ARG
+    assert _call_decode(lib, plb, odt=_lib.MLA_OUT_FP8_E4M3) == _lib.MLA_ERR_INVALID_ARG
