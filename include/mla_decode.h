@@ -155,9 +155,15 @@ mla_status_t mla_decode(const mla_decode_plan_t* plan, const void* q_nope, int64
  * mla_split_kv -- the first stage alone (paged KV gather, QK^T, online
  * softmax with the causal mask, PV, split epilogue); the per-split partial of
  * width kv_lora_rank + 1 follows the attn_logits layout of the vLLM PR #46819
- * summary (key code excerpt).  Same arguments as mla_decode.  With one split it writes out/lse directly; otherwise it writes
- * the fp32 partials [B, q_len, H, splits, 513] (512 normalised outputs, then
- * the split's LSE; an empty split writes 0 and -inf) into the workspace.
+ * summary (key code excerpt).  Same arguments as mla_decode.
+ *
+ * Request b uses s_b = clamp(ceil(L_b / chunk_tokens), 1, num_kv_splits)
+ * splits.  With s_b = 1 the stage writes the request's out/lse directly (and,
+ * when the plan has more splits, +inf as the LSE of its first partial, which
+ * tells mla_combine to leave those rows alone).  Otherwise it writes fp32
+ * partials [B, q_len, H, splits, 513] into the workspace: for splits below s_b
+ * the 512 normalised outputs and the split's LSE (-inf if no row of the split
+ * sees a token), for the others only an LSE of -inf.
  */
 mla_status_t mla_split_kv(const mla_decode_plan_t* plan, const void* q_nope,
                           int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,

@@ -6,7 +6,10 @@
 //   M   = max_s lse_s
 //   lse = M + ln sum_s exp(lse_s - M)
 //   out = sum_s exp(lse_s - lse) * o_s
-// Empty splits carry lse_s = -inf and weigh zero (a row whose splits are all
+// Empty splits carry lse_s = -inf and weigh zero; their outputs are not read
+// (the split kernel writes only the LSE of a split past a request's end).  A
+// row whose first LSE is +inf belongs to a request with a single split, whose
+// output the split kernel already wrote.  (A row whose splits are all
 // empty, which only a sequence shard can have, gets out = 0 and lse = -inf).
 // The same merge joins the partials of sequence shards gathered from several
 // ranks, read with their own row and split strides.  One warp per row; each lane
@@ -37,6 +40,9 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams
   if (row >= (int64_t)p.batch * p.rows) return;
   const float* part = p.partials + row * p.part_row_stride;
   const int64_t sstride = p.part_split_stride;
+  // +inf in the first partial's LSE: the request had a single split and the
+  // split kernel wrote this row's out/lse itself.
+  if (part[kKvLora] == INFINITY) return;
 
   // Pass 1: the largest split LSE (NaN marks a request the split kernel rejected).
   float M = -INFINITY;

@@ -345,6 +345,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   const int b = ctl->req;
 
   const int L = lpt ? lens[b] : p.seq_lens[b];  // tokens of request b in this cache
+  const int row0 = rg * kRows;
+  const int64_t grow0 = (int64_t)b * p.rows + row0;
+  // Splits of this request: those whose chunk starts before L (at least one,
+  // at most the plan's).  With a single one the cluster of split 0 writes the
+  // final out/lse itself; a split past the request's end only marks its
+  // partial rows empty for the combine (their outputs are never read) and
+  // leaves.  The combine applies the same rule.
+  const int nsb = (int)max((int64_t)1, min((int64_t)p.splits, ((int64_t)L + p.chunk_tokens - 1) / p.chunk_tokens));
+  if (split >= nsb) {
+    if (cta == 0 && (int)threadIdx.x < min(kRows, p.rows - row0))
+      p.partials[((grow0 + threadIdx.x) * p.splits + split) * kPartRow + kKvLora] = -INFINITY;
+    if (warp == 0) tmem_dealloc(ctl->tmem_base, kTmemCols);
+    return;
+  }
   // This request's query tokens: rows (b, i, h) with i >= qlb are padding of a
   // per-request q_len call, computed fully masked (out 0, lse -inf).
   const int qlb = p.q_lens ? p.q_lens[b] : p.q_len;
@@ -360,7 +374,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   const int hi = len_ok ? min(lo + p.chunk_tokens, L) : lo;
   const int first_page = lo / kPage;
   const int n_pages = hi > lo ? (hi + kPage - 1) / kPage - first_page : 0;
-  const int row0 = rg * kRows;
   const float kv_scale = (kFp8 && p.kv_scale) ? *p.kv_scale : 1.0f;
   const float q_scale = (kQ8 && p.q_scale) ? *p.q_scale : 1.0f;  // folded into the softmax scale
   const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride + first_page;
@@ -1052,11 +1065,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     const float l_tot = l_sum + ctl->l_peer[r];
     const bool has = l_tot > 0.f;
     const float il = has ? kv_scale / l_tot : 0.f;
-    const int64_t grow0 = (int64_t)b * p.rows + row0;
     if (cta == 0 && row_ok) {
       const float lv = bad ? NAN : (has ? (r_ref + lg2(l_tot)) * kLn2 : -INFINITY);
-      if (p.splits == 1) {
+      if (nsb == 1) {
         if (p.lse) p.lse[(grow0 + r) * p.lse_stride] = lv;
+        // +inf (never a real LSE) in split 0's slot: the combine leaves the row alone
+        if (p.splits > 1) p.partials[(grow0 + r) * p.splits * kPartRow + kKvLora] = INFINITY;
       } else {
         p.partials[((grow0 + r) * p.splits + split) * kPartRow + kKvLora] = lv;
       }
@@ -1109,7 +1123,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       __syncwarp();  // the tile may be rewritten once every lane holds its column
       const int dim = (int)cta * 256 + c0 + lane;
       const int nr = min(32, rows_here - quad * 32);  // rows of this warp that exist
-      if (p.splits > 1) {
+      if (nsb > 1) {
         float* dst = p.partials + ((grow0 + quad * 32) * p.splits + split) * kPartRow + dim;
         const int64_t step = (int64_t)p.splits * kPartRow;
 #pragma unroll
