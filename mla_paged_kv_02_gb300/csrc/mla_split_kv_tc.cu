@@ -216,6 +216,12 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
+// Splits request b uses: those whose chunk starts before its L tokens, at least
+// one and at most the plan's (the combine applies the same rule).
+__device__ __forceinline__ int request_splits(const DecodeParams& p, int L) {
+  return (int)max((int64_t)1, min((int64_t)p.splits, ((int64_t)L + p.chunk_tokens - 1) / p.chunk_tokens));
+}
+
 // Bounded wait that also gives up once any role of this CTA has aborted.  CTA
 // scope suffices for every barrier completed by local arrives, by transaction
 // bytes (TMA, st.async, bulk copies) or by a relaxed "consumed" signal; only a
@@ -346,16 +352,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
 
   const int L = lpt ? lens[b] : p.seq_lens[b];  // tokens of request b in this cache
   const int row0 = rg * kRows;
-  const int64_t grow0 = (int64_t)b * p.rows + row0;
   // Splits of this request: those whose chunk starts before L (at least one,
   // at most the plan's).  With a single one the cluster of split 0 writes the
   // final out/lse itself; a split past the request's end only marks its
   // partial rows empty for the combine (their outputs are never read) and
   // leaves.  The combine applies the same rule.
-  const int nsb = (int)max((int64_t)1, min((int64_t)p.splits, ((int64_t)L + p.chunk_tokens - 1) / p.chunk_tokens));
-  if (split >= nsb) {
+  if (split >= request_splits(p, L)) {
     if (cta == 0 && (int)threadIdx.x < min(kRows, p.rows - row0))
-      p.partials[((grow0 + threadIdx.x) * p.splits + split) * kPartRow + kKvLora] = -INFINITY;
+      p.partials[(((int64_t)b * p.rows + row0 + threadIdx.x) * p.splits + split) * kPartRow + kKvLora] = -INFINITY;
     if (warp == 0) tmem_dealloc(ctl->tmem_base, kTmemCols);
     return;
   }
@@ -740,7 +744,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     const bool row_ok = row0 + r < p.rows;   // the row exists (it is written)
     const int qi = (row0 + r) / p.num_heads;
     const bool row_live = row_ok && qi < qlb;  // not padding of a per-request q_len
-    const int vis = Ltot - qlb + 1 + qi - kv0;  // tokens of this cache the row may see
+    // Tokens of this cache the row may see: its causal limit in this cache's
+    // positions, and never past the cache's own L (a shard's range can end
+    // before the row's limit).
+    const int vis = min(Ltot - qlb + 1 + qi - kv0, L);
     const float sc2 = p.softmax_scale * kv_scale * q_scale * kLog2e;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t col_own = kColS + 32 * cta;    // S columns of this CTA's token half (within a buffer)
@@ -1065,6 +1072,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     const float l_tot = l_sum + ctl->l_peer[r];
     const bool has = l_tot > 0.f;
     const float il = has ? kv_scale / l_tot : 0.f;
+    const int64_t grow0 = (int64_t)b * p.rows + row0;
+    const int nsb = request_splits(p, L);
     if (cta == 0 && row_ok) {
       const float lv = bad ? NAN : (has ? (r_ref + lg2(l_tot)) * kLn2 : -INFINITY);
       if (nsb == 1) {
