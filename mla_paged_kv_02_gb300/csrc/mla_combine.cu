@@ -40,18 +40,20 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams
   if (row >= (int64_t)p.batch * p.rows) return;
   const float* part = p.partials + row * p.part_row_stride;
   const int64_t sstride = p.part_split_stride;
-  // +inf in the first partial's LSE: the request had a single split and the
-  // split kernel wrote this row's out/lse itself.
-  if (part[kKvLora] == INFINITY) return;
 
   // Pass 1: the largest split LSE (NaN marks a request the split kernel rejected).
   float M = -INFINITY;
   bool nan_seen = false;
+  bool single = false;
   for (int s = lane; s < p.splits; s += 32) {
     const float v = part[(int64_t)s * sstride + kKvLora];
+    // +inf in the first partial's LSE: the request had a single split and the
+    // split kernel wrote this row's out/lse itself.
+    single |= (s == 0) & (v == INFINITY);
     nan_seen |= (v != v);
     M = fmaxf(M, v);
   }
+  if (__any_sync(0xffffffffu, single)) return;
   M = warp_max(M);
   nan_seen = __any_sync(0xffffffffu, nan_seen);
 

@@ -125,8 +125,15 @@ template <bool kFp8>
 __host__ __device__ constexpr int send_warp0() { return kFp8 ? 10 : 6; }  // S sender warps
 template <bool kFp8>
 __host__ __device__ constexpr int pv_warp() { return kFp8 ? 14 : 10; }
+// L2 prefetch distance in pages (0: no prefetch warp).  See the prefetch warp.
+#ifndef MLA_PREFETCH_AHEAD
+#define MLA_PREFETCH_AHEAD 0
+#endif
+constexpr int kPrefetchAhead = MLA_PREFETCH_AHEAD;
 template <bool kFp8>
-__host__ __device__ constexpr int block_threads() { return 32 * (pv_warp<kFp8>() + 1); }
+__host__ __device__ constexpr int pf_warp() { return pv_warp<kFp8>() + 1; }
+template <bool kFp8>
+__host__ __device__ constexpr int block_threads() { return 32 * (pv_warp<kFp8>() + 1 + (kPrefetchAhead > 0 ? 1 : 0)); }
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -167,6 +174,7 @@ struct Ctl {
   uint64_t drain;
   uint32_t tmem_base;
   int req;                     // the request this cluster works on
+  int loaded;                  // pages whose TMA load the producer has issued (read by the prefetch warp)
   int abort;
   int poisoned;
   float u_peer[2][kRows];      // [P buffer][row]: reference the peer computed its half with
@@ -309,6 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     mbar_init(&ctl->fin, 4);
     mbar_init(&ctl->drain, 2);  // both MMA-issuing threads' last commits
     ctl->abort = 0;
+    ctl->loaded = 0;
     fence_mbarrier_init();
   }
 
@@ -453,6 +462,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
           tma_load_2d(stage + 4 * kKvChunkBytes, &tm_kpe, land, 8 * 64 + 32 * (int)cta, page * kPage);
         }
         issued = j + 1;
+        if (kPrefetchAhead > 0) *(volatile int*)&ctl->loaded = issued;
       }
       // Never leave with copies in flight.
       for (int j = max(0, issued - kNS); j < issued; ++j) {
@@ -573,6 +583,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(smem_u32(&ctl->drain), 0))
         if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  } else if (kPrefetchAhead > 0 && warp == pf_warp<kFp8>()) {
+    // ------------------------------------------------------------ L2 prefetch
+    // The CTA's columns of page j are requested into L2 once the producer has
+    // issued the TMA load of page j - kPrefetchAhead, so that page j's own
+    // load, issued when its ring stage frees, finds the bytes in L2 instead of
+    // HBM (a shorter load -> QK -> ... -> PV chain per ring stage).  Plain
+    // per-lane prefetches through the L1/L2 path, not the copy engine that
+    // carries the pair's transfers.  A hint only: on an abort, or when the
+    // producer stops making progress, it gives up without reporting anything.
+    const int eb = kFp8 ? 1 : 2;  // bytes per element
+    for (int j = kNS; j < n_pages; ++j) {
+      const int need = j - kPrefetchAhead + 1;
+      bool go = true;
+      if (need > 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (*(volatile int*)&ctl->loaded < need) {
+          if (*(volatile int*)&ctl->abort || globaltimer_ns() - t0 > kWaitLimitNs) {
+            go = false;
+            break;
+          }
+          __nanosleep(256);
+        }
+      }
+      if (!__all_sync(0xffffffffu, go)) break;
+      const int page = bt_row[j];
+      if (page < 0 || page >= p.num_pages) continue;
+      const char* base = static_cast<const char*>(p.kv) + (int64_t)page * kPage * kRow * eb;
+      for (int t = lane; t < kPage; t += 32) {
+        const char* row = base + (int64_t)t * kRow * eb;
+#pragma unroll
+        for (int l = 0; l < 256 * eb / 128; ++l) prefetch_l2(row + 256 * (int)cta * eb + 128 * l);
+        prefetch_l2(row + (kKvLora + 32 * (int)cta) * eb);  // the k_pe columns
+      }
     }
   } else if (kQ8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
     // ------------------------------------------------------------ e4m3 -> bf16 V (FP8 query)
