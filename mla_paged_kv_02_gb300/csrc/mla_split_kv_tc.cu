@@ -50,6 +50,8 @@
 // TMEM: O_c at columns [0,256), S double buffer at [256,384), Q at [384,512).
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx_sm100.cuh"
@@ -125,15 +127,8 @@ template <bool kFp8>
 __host__ __device__ constexpr int send_warp0() { return kFp8 ? 10 : 6; }  // S sender warps
 template <bool kFp8>
 __host__ __device__ constexpr int pv_warp() { return kFp8 ? 14 : 10; }
-// L2 prefetch distance in pages (0: no prefetch warp).  See the prefetch warp.
-#ifndef MLA_PREFETCH_AHEAD
-#define MLA_PREFETCH_AHEAD 0
-#endif
-constexpr int kPrefetchAhead = MLA_PREFETCH_AHEAD;
 template <bool kFp8>
-__host__ __device__ constexpr int pf_warp() { return pv_warp<kFp8>() + 1; }
-template <bool kFp8>
-__host__ __device__ constexpr int block_threads() { return 32 * (pv_warp<kFp8>() + 1 + (kPrefetchAhead > 0 ? 1 : 0)); }
+__host__ __device__ constexpr int block_threads() { return 32 * (pv_warp<kFp8>() + 1); }
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -174,7 +169,6 @@ struct Ctl {
   uint64_t drain;
   uint32_t tmem_base;
   int req;                     // the request this cluster works on
-  int loaded;                  // pages whose TMA load the producer has issued (read by the prefetch warp)
   int abort;
   int poisoned;
   float u_peer[2][kRows];      // [P buffer][row]: reference the peer computed its half with
@@ -317,7 +311,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     mbar_init(&ctl->fin, 4);
     mbar_init(&ctl->drain, 2);  // both MMA-issuing threads' last commits
     ctl->abort = 0;
-    ctl->loaded = 0;
     fence_mbarrier_init();
   }
 
@@ -462,7 +455,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
           tma_load_2d(stage + 4 * kKvChunkBytes, &tm_kpe, land, 8 * 64 + 32 * (int)cta, page * kPage);
         }
         issued = j + 1;
-        if (kPrefetchAhead > 0) *(volatile int*)&ctl->loaded = issued;
       }
       // Never leave with copies in flight.
       for (int j = max(0, issued - kNS); j < issued; ++j) {
@@ -478,7 +470,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // thread of its own (below), so a PV that becomes ready never waits behind
     // the issue of a QK; the stage ring, S, S_in and P barriers bound how far QK
     // runs ahead.
-    if (lane == 0 && n_pages > 0 && kQ8) {
+    if constexpr (kQ8) {
+     if (lane == 0 && n_pages > 0) {
       // FP8 query: QK(j) on the page's e4m3 codes as soon as they land (the
       // converter's bf16 V is only needed by PV): 8 K-steps of 32 codes over the
       // two c_kv boxes, A from tensor memory, and one over the 32 k_pe codes, A
@@ -510,6 +503,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(smem_u32(&ctl->drain), 0))
         if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+     }
     } else if (lane == 0 && n_pages > 0) {
       const uint32_t kv_addr = smem_u32(sKV);
       const uint64_t qpe_desc = sdesc_sw64(smem_u32(sQpe), 16, 512);
@@ -584,49 +578,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       while (!mbar_try_wait(smem_u32(&ctl->drain), 0))
         if (globaltimer_ns() - t0 > kWaitLimitNs) break;
     }
-  } else if (kPrefetchAhead > 0 && warp == pf_warp<kFp8>()) {
-    // ------------------------------------------------------------ L2 prefetch
-    // The CTA's columns of page j are requested into L2 once the producer has
-    // issued the TMA load of page j - kPrefetchAhead, so that page j's own
-    // load, issued when its ring stage frees, finds the bytes in L2 instead of
-    // HBM (a shorter load -> QK -> ... -> PV chain per ring stage).  Plain
-    // per-lane prefetches through the L1/L2 path, not the copy engine that
-    // carries the pair's transfers.  A hint only: on an abort, or when the
-    // producer stops making progress, it gives up without reporting anything.
-    const int eb = kFp8 ? 1 : 2;  // bytes per element
-    for (int j = kNS; j < n_pages; ++j) {
-      const int need = j - kPrefetchAhead + 1;
-      bool go = true;
-      if (need > 0) {
-        const uint64_t t0 = globaltimer_ns();
-        while (*(volatile int*)&ctl->loaded < need) {
-          if (*(volatile int*)&ctl->abort || globaltimer_ns() - t0 > kWaitLimitNs) {
-            go = false;
-            break;
-          }
-          __nanosleep(256);
-        }
-      }
-      if (!__all_sync(0xffffffffu, go)) break;
-      const int page = bt_row[j];
-      if (page < 0 || page >= p.num_pages) continue;
-      const char* base = static_cast<const char*>(p.kv) + (int64_t)page * kPage * kRow * eb;
-      for (int t = lane; t < kPage; t += 32) {
-        const char* row = base + (int64_t)t * kRow * eb;
-#pragma unroll
-        for (int l = 0; l < 256 * eb / 128; ++l) prefetch_l2(row + 256 * (int)cta * eb + 128 * l);
-        prefetch_l2(row + (kKvLora + 32 * (int)cta) * eb);  // the k_pe columns
-      }
-    }
   } else if (kQ8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
     // ------------------------------------------------------------ e4m3 -> bf16 V (FP8 query)
-    // Thread ct converts token ct/2 of c_kv box ct%2 (128 codes, 128B-swizzled)
-    // into bf16 V chunks 2(ct%2) and 2(ct%2)+1, writing zeros for tokens at or
-    // past L and for a page that was never loaded (such slots may hold
-    // anything).  Box 1's bf16 output covers the codes QK reads, so it is
-    // written only once QK of the page has completed.
+    // Warps 0-1 of the group convert c_kv box 0 and warps 2-3 box 1: thread ct
+    // takes token ct%64 (128 codes, 128B-swizzled) into bf16 V chunks 2h and
+    // 2h+1 (h = ct/64), writing zeros for tokens at or past L and for a page
+    // that was never loaded (such slots may hold anything).  Box 1's bf16
+    // output covers the codes QK reads, so its warps first wait for QK of the
+    // page to complete.  One copy of the conversion code serves both boxes.
     const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
-    const int t = ct >> 1, h = ct & 1;
+    const int t = ct & 63, h = ct >> 6;
     int page_next = n_pages > 0 ? bt_row[0] : 0;
     for (int j = 0; j < n_pages; ++j) {
       const int st = j % kNS;
@@ -640,33 +601,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       const uint8_t* src = stage + kQ8RawOff + h * kQ8Box + t * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u) raw[u] = *reinterpret_cast<const uint4*>(src + ((u ^ (t & 7)) << 4));
+      conv_sync();  // every thread holds its codes before box 1's space is rewritten
+      const bool ok = h == 0 || __all_sync(0xffffffffu, wait_bar(ctl, &ctl->qk_done[st], (j / kNS) & 1, p, 25));
       // Logical 16-code piece u of the row: bf16 chunk 2h + u/4, 16-byte units
       // 2(u%4) and 2(u%4)+1 of token row t (128B swizzle).
-      auto write = [&]() {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint8_t* dst = stage + (2 * h + (u >> 2)) * kKvChunkBytes + t * 128;
-          const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-          uint32_t o[8];
+      for (int u = 0; u < 8; ++u) {
+        uint8_t* dst = stage + (2 * h + (u >> 2)) * kKvChunkBytes + t * 128;
+        const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+        uint32_t o[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            o[2 * q] = zero ? 0u : e4m3x2_to_bf16x2((uint16_t)(w[q] & 0xFFFFu));
-            o[2 * q + 1] = zero ? 0u : e4m3x2_to_bf16x2((uint16_t)(w[q] >> 16));
-          }
-          const int c0 = 2 * (u & 3);
-          *reinterpret_cast<uint4*>(dst + ((c0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        for (int q = 0; q < 4; ++q) {
+          o[2 * q] = zero ? 0u : e4m3x2_to_bf16x2((uint16_t)(w[q] & 0xFFFFu));
+          o[2 * q + 1] = zero ? 0u : e4m3x2_to_bf16x2((uint16_t)(w[q] >> 16));
         }
-      };
-      conv_sync();  // every thread holds its codes before box 1's space is rewritten
-      if (h == 0) write();
-      if (conv_sync_or(!wait_bar(ctl, &ctl->qk_done[st], (j / kNS) & 1, p, 25))) break;
-      if (h == 1) write();
+        const int c0 = 2 * (u & 3);
+        *reinterpret_cast<uint4*>(dst + ((c0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      if (conv_sync_or(!ok)) break;
       fence_proxy_async_smem();
       conv_sync();
       if (lane == 0) mbar_arrive(&ctl->full[st]);
     }
-  } else if (kFp8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
+  } else if (kFp8 && !kQ8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
     // ------------------------------------------------------------ e4m3 -> bf16 converter
     // Thread ct converts tokens ct/2 of chunks 2(ct%2) and 2(ct%2)+1 (64 e4m3
     // bytes each, into 128-byte swizzled bf16 rows), and threads below 64 also
@@ -1182,22 +1140,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr)
           if (rr < nr) dst[rr * step] = col[rr];
-      } else if (p.out_fp32) {
+      } else if (p.out_fp32 && p.out_stride == kKvLora) {
+        float* dst = reinterpret_cast<float*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr)
+          if (rr < nr) dst[rr * kKvLora] = col[rr];
+      } else if (p.out_fp32) {  // 513-wide partial rows of a sequence shard
         float* dst = reinterpret_cast<float*>(p.out) + (grow0 + quad * 32) * p.out_stride + dim;
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr)
           if (rr < nr) dst[rr * p.out_stride] = col[rr];
-      } else if (p.out_fp8) {
+      } else if (p.out_fp8) {  // (bf16 and e4m3 outputs always have 512-wide rows)
         const float osc = p.out_scale ? *p.out_scale : 1.f;
-        uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) + (grow0 + quad * 32) * p.out_stride + dim;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr)
-          if (rr < nr) dst[rr * p.out_stride] = to_e4m3(col[rr], osc);
+          if (rr < nr) dst[rr * kKvLora] = to_e4m3(col[rr], osc);
       } else {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (grow0 + quad * 32) * p.out_stride + dim;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (grow0 + quad * 32) * kKvLora + dim;
 #pragma unroll
         for (int rr = 0; rr < 32; ++rr)
-          if (rr < nr) dst[rr * p.out_stride] = __float2bfloat16_rn(col[rr]);
+          if (rr < nr) dst[rr * kKvLora] = __float2bfloat16_rn(col[rr]);
       }
     }
     tc_fence_before();
@@ -1268,8 +1231,19 @@ cudaError_t launch_kernel(const dim3& grid, const CUtensorMap& tm_qn, const CUte
                           const DecodeParams& p, cudaStream_t stream) {
   auto kern = split_kv_tc_kernel<kFp8, kQ8>;
   constexpr int kSmem = Layout<kFp8>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  // The shared-memory opt-in is a property of the kernel in the device's
+  // context: set once per device (a bit per device; a lost race only repeats
+  // the same idempotent call).
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit, std::memory_order_release);
+  }
   kern<<<grid, block_threads<kFp8>(), kSmem, stream>>>(tm_qn, tm_qp, tm_kv, tm_kv3, tm_kpe, p);
   return cudaGetLastError();
 }
