@@ -20,6 +20,9 @@ constexpr int kRowsPerCta = 128;
 constexpr int kCtasPerGroup = 2;
 constexpr int kMaxSplits = 256;
 constexpr double kSetupPages = 2.0;
+// Fixed cost of the combine kernel (launch, and the dependent loads of a row's
+// split LSEs), in page-times: about 10 us measured even for a tiny batch.
+constexpr double kCombinePages = 8.0;
 // The split kernel's grid is (2 * row_groups, splits, batch): the splits and
 // the batch sit on gridDim.y and gridDim.z, whose hardware limit is 65535.
 constexpr int kMaxGridYZ = 65535;
@@ -167,8 +170,9 @@ mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_le
     if (splits > kMaxGridYZ) splits = kMaxGridYZ;
   } else {
     // Smallest modelled time: whole waves of one-CTA-per-SM work, each CTA paying
-    // its pages plus a fixed set-up, plus the partial write+read (and combine launch)
-    // when there is more than one split, all in per-SM page-times.
+    // its pages plus a fixed set-up, plus the partial write+read and the combine
+    // kernel's fixed cost when there is more than one split, all in per-SM
+    // page-times.
     double best = 1e300;
     const int smax = pages < kMaxSplits ? pages : kMaxSplits;
     for (int s = 1; s <= smax; ++s) {
@@ -178,7 +182,7 @@ mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_le
       double cost = (double)waves * (ppc + kSetupPages);
       if (s > 1) {
         const double pbytes = 2.0 * batch * rows * (double)s * (MLA_KV_LORA_RANK + 1) * 4.0;
-        cost += pbytes / (num_sms * page_bytes) + kSetupPages;
+        cost += pbytes / (num_sms * page_bytes) + kCombinePages;
       }
       if (cost < best * (1.0 - 1e-9)) {
         best = cost;
