@@ -1,8 +1,8 @@
 """Benchmark: MLA decode (absorbed form, paged latent KV cache) on GB300.
 
-One step = one full decode call (the split-KV attention kernel, whose last
-cluster per request merges the splits) over the resident synthetic MTP-3
-workload (B=64, H=32, q_len=4, kv_len=81920, page 64, bf16 cache).  The KV stream (6.04 GB) is larger than L2, so no flush
+One step = one full decode call (split-KV attention kernel + LSE combine) over
+the resident synthetic MTP-3 workload (B=64, H=32, q_len=4, kv_len=81920,
+page 64, bf16 cache).  The KV stream (6.04 GB) is larger than L2, so no flush
 is needed between timed steps.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -268,21 +268,24 @@ def main():
     qn, qp = inp.q_nope.view(-1, 512), inp.q_pe.view(-1, 64)
 
     def call(qn_, qp_, bt_, sl_, ev=None):
-        """One decode through the public C call (mla_decode, or mla_decode_fp8 for an
-        FP8 query): one split-KV kernel whose last cluster per request merges the
-        splits, preceded by a zeroing of the merge counters when there are splits.
-        With events, [0]-[1] brackets the whole call."""
+        """One decode; with events, [0]-[1] brackets the split kernel and [1]-[2] the
+        combine (an FP8-query call is one C call: [0]-[1] brackets both)."""
         if ev:
             ev[0].record(stream)
         if q8:
             st = _lib.decode_fp8(pl, qn_, qp_, qs, inp.kv_cache, bt_, sl_, inp.softmax_scale, kvs, out, None, lse,
                                  ws, stream)
+            st2 = 0
+            if ev:
+                ev[1].record(stream)
         else:
-            st = _lib.decode(pl, qn_, qp_, inp.kv_cache, bt_, sl_, inp.softmax_scale, kvs, out, lse, ws, stream)
+            st = _lib.split_kv(pl, qn_, qp_, inp.kv_cache, bt_, sl_, inp.softmax_scale, kvs, out, lse, ws, stream)
+            if ev:
+                ev[1].record(stream)
+            st2 = _lib.combine(pl, out, lse, ws, stream)
         if ev:
-            ev[1].record(stream)
             ev[2].record(stream)
-        assert st == 0, st
+        assert st == 0 and st2 == 0, (st, st2)
 
     def step(ev=None):
         call(qn, qp, inp.block_table, inp.seq_lens, ev)
@@ -377,7 +380,7 @@ def main():
         floor_s = 1152 * pairs / (2 * tc_peak * 1e12) + 1024 * pairs / (tc_peak * 1e12)
         eff_peak = aflops / floor_s / 1e12
         tc = {"achieved": achieved_tf, "peak": eff_peak, "unit": "TFLOP/s", "frac": achieved_tf / eff_peak,
-              "peak_note": "QK at 2x measured bf16 (fp8), PV at measured bf16"}
+              "peak_note": "QK at 2x measured bf16 (fp8), PV at measured bf16; timed split+combine"}
     if aflops / (tc["peak"] * 1e12) > abytes / (hbm_peak * 1e9):
         roofline = {"bound": "tensor", **tc, "traffic": traffic, "peak_source": peak_kind, "hbm": hbm}
     else:
@@ -399,10 +402,10 @@ def main():
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "gb_per_s": abytes * world / (step_us * 1e-6) / 1e9,
         "tflops": aflops * world / (step_us * 1e-6) / 1e12,
-        "kernel_us": {"split_kv_with_merge": split_us},
+        "kernel_us": ({"split_kv+combine": split_us} if q8 else {"split_kv": split_us, "combine": comb_us}),
         "roofline": roofline,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (1 + (pl.num_kv_splits > 1)),
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -68,7 +68,7 @@ typedef struct {
     int row_groups;      /* ceil(num_heads * q_len / rows_per_cta)                      */
     int reserved[3];
     size_t partial_bytes;   /* fp32 split partials [B, q_len, H, splits, 513]; 0 if 1 split */
-    size_t workspace_bytes; /* header + merge counters + partials (none of either with one split) */
+    size_t workspace_bytes; /* header + partials                                        */
 } mla_decode_plan_t;
 
 /*
@@ -112,11 +112,8 @@ mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_le
 mla_status_t mla_workspace_init(void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
- * mla_decode -- the whole decode in one split-KV attention kernel: when a
- * request uses more than one split, the last of its clusters to finish merges
- * the splits' partials (the LSE-weighted combine) before it exits, so no
- * second kernel runs; a few hundred bytes of merge counters in the workspace
- * are zeroed on the stream first.  The operation is
+ * mla_decode -- the whole decode: the split-KV attention kernel, then (when
+ * plan->num_kv_splits > 1) the LSE-weighted combine kernel.  The operation is
  * the absorbed-form decode at the top of this header; the call shape (query
  * parts, paged cache, block table, lengths, per-call scales, out + lse) is
  * the TokenSpeed MLA summary's decode interface (vLLM PR #41778,
@@ -159,9 +156,6 @@ mla_status_t mla_decode(const mla_decode_plan_t* plan, const void* q_nope, int64
  * softmax with the causal mask, PV, split epilogue); the per-split partial of
  * width kv_lora_rank + 1 follows the attn_logits layout of the vLLM PR #46819
  * summary (key code excerpt).  Same arguments as mla_decode.
- *
- * This stage and mla_combine are the decode taken apart, for callers that
- * want the two kernels separately; mla_decode runs both in one kernel.
  *
  * Request b uses s_b = clamp(ceil(L_b / chunk_tokens), 1, num_kv_splits)
  * splits.  With s_b = 1 the stage writes the request's out/lse directly (and,

@@ -54,10 +54,6 @@ struct DecodeParams {
   // partials it reads ([rows, splits, 513] in the workspace; [splits, rows, 513]
   // for gathered shard partials).
   int64_t part_row_stride, part_split_stride;
-  // Split kernel: the last cluster of a request to finish merges its splits
-  // (arrivals: one counter per (request, row group), zero before the launch).
-  int fuse_merge;
-  int* arrivals;
   int32_t* err;     // workspace header
   int batch, num_heads, q_len, rows;  // rows = num_heads * q_len per request
   int max_seq_len, splits, chunk_tokens, rows_per_cta, row_groups;
@@ -94,67 +90,6 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t row, in
     reinterpret_cast<uint8_t*>(p.out)[row * p.out_stride + d] = to_e4m3(v, out_scale);
   else
     reinterpret_cast<__nv_bfloat16*>(p.out)[row * p.out_stride + d] = __float2bfloat16_rn(v);
-}
-
-__device__ __forceinline__ float warp_max_f(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum_f(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// LSE merge of one row's split partials by one warp (the combine of the split
-// partial layout [.., splits, 513]; vLLM PR #46819 summary, key code excerpt):
-//   M = max_s lse_s,  lse = M + ln sum_s exp(lse_s - M),
-//   out = sum_s exp(lse_s - lse) * o_s.
-// `part` points at the row's first partial, `sstride` floats between splits.
-// Splits with lse = -inf weigh nothing and their outputs are not read; a NaN
-// LSE (a request the split kernel rejected) makes the row NaN; a row whose
-// splits are all empty gets out = 0 and lse = -inf.  Each lane owns 16 of the
-// 512 columns.  The loads bypass L1 (the partials may have been written by
-// other SMs of the same kernel).
-__device__ __forceinline__ void merge_row(const DecodeParams& p, int64_t row, const float* part, int64_t sstride,
-                                          int nsplit, float out_scale) {
-  const int lane = threadIdx.x & 31;
-  float M = -INFINITY;
-  bool nan_seen = false;
-  for (int s = lane; s < nsplit; s += 32) {
-    const float v = __ldcg(part + (int64_t)s * sstride + kKvLora);
-    nan_seen |= (v != v);
-    M = fmaxf(M, v);
-  }
-  M = warp_max_f(M);
-  nan_seen = __any_sync(0xffffffffu, nan_seen);
-  float acc = 0.f;
-  for (int s = lane; s < nsplit; s += 32) {
-    const float v = __ldcg(part + (int64_t)s * sstride + kKvLora);
-    acc += (v == -INFINITY) ? 0.f : __expf(v - M);
-  }
-  acc = warp_sum_f(acc);
-  const float lse = (M == -INFINITY || nan_seen) ? (nan_seen ? NAN : -INFINITY) : M + logf(acc);
-  float o[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) o[k] = 0.f;
-  if (!nan_seen && M != -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const float* ps = part + (int64_t)s * sstride;
-      const float v = __ldcg(ps + kKvLora);
-      if (v == -INFINITY) continue;
-      const float w = __expf(v - lse);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) o[k] = fmaf(w, __ldcg(ps + lane + 32 * k), o[k]);
-    }
-  } else if (nan_seen) {
-#pragma unroll
-    for (int k = 0; k < 16; ++k) o[k] = NAN;
-  }
-#pragma unroll
-  for (int k = 0; k < 16; ++k) store_out(p, row, lane + 32 * k, o[k], out_scale);
-  if (p.lse && lane == 0) p.lse[row * p.lse_stride] = lse;
 }
 
 }  // namespace mla

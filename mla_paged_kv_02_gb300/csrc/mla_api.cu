@@ -37,18 +37,6 @@ size_t partial_bytes_for(int64_t batch, int64_t rows, int64_t splits) {
   return splits > 1 ? (size_t)(batch * rows * splits * (MLA_KV_LORA_RANK + 1)) * sizeof(float) : 0;
 }
 
-// Bytes of the arrival counters (one int per request and row group, rounded up
-// to 256 bytes) that let the last cluster of a request merge its splits;
-// none with one split.
-size_t arrival_bytes_for(int64_t batch, int64_t row_groups, int64_t splits) {
-  return splits > 1 ? (size_t)((batch * row_groups * 4 + 255) / 256 * 256) : 0;
-}
-
-// Workspace layout: header | arrival counters | partials.
-size_t partials_offset(const mla_decode_plan_t* pl) {
-  return MLA_WORKSPACE_HEADER_BYTES + arrival_bytes_for(pl->batch, pl->row_groups, pl->num_kv_splits);
-}
-
 // A plan is usable only if every field is the planner's own arithmetic: the
 // kernels size their writes from num_kv_splits, so a plan whose byte counts do
 // not follow from its shape (edited after mla_decode_plan, or never planned)
@@ -66,26 +54,12 @@ bool plan_ok(const mla_decode_plan_t* pl) {
         (int64_t)(pl->num_kv_splits - 1) * pl->chunk_tokens < pl->max_seq_len))
     return false;
   const size_t part = partial_bytes_for(pl->batch, (int64_t)pl->num_heads * pl->q_len, pl->num_kv_splits);
-  return pl->partial_bytes == part && pl->workspace_bytes == partials_offset(pl) + part;
+  return pl->partial_bytes == part && pl->workspace_bytes == MLA_WORKSPACE_HEADER_BYTES + part;
 }
 
 #ifdef MLA_DEBUG
 uint64_t g_debug_wait_limit_ns = 0;  // 0: the kernels' built-in limit
 #endif
-
-// The whole decode in one kernel: with more than one split the arrival
-// counters are zeroed first (they sit where another plan may have left
-// partials), and the last cluster of each request merges its splits.
-mla_status_t launch_fused(DecodeParams& p, const mla_decode_plan_t* pl, cudaStream_t stream) {
-  p.fuse_merge = 1;
-  const size_t arrival_bytes = arrival_bytes_for(pl->batch, pl->row_groups, pl->num_kv_splits);
-  if (arrival_bytes && cudaMemsetAsync(p.arrivals, 0, arrival_bytes, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return MLA_ERR_CUDA;
-  }
-  if (launch_split_kv(p, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  return MLA_OK;
-}
 
 }  // namespace
 
@@ -141,8 +115,7 @@ mla_status_t fill_params(const mla_decode_plan_t* pl, const void* q_nope, int64_
   p->lse = lse;
   p->lse_stride = 1;
   p->err = static_cast<int32_t*>(workspace);
-  p->arrivals = reinterpret_cast<int*>(static_cast<char*>(workspace) + MLA_WORKSPACE_HEADER_BYTES);
-  p->partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + partials_offset(pl));
+  p->partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + MLA_WORKSPACE_HEADER_BYTES);
   p->batch = pl->batch;
   p->num_heads = pl->num_heads;
   p->q_len = pl->q_len;
@@ -232,7 +205,7 @@ mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_le
   plan->rows_per_cta = kRowsPerCta;
   plan->row_groups = row_groups;
   plan->partial_bytes = partial_bytes_for(batch, rows, splits);
-  plan->workspace_bytes = partials_offset(plan) + plan->partial_bytes;
+  plan->workspace_bytes = MLA_WORKSPACE_HEADER_BYTES + plan->partial_bytes;
   return MLA_OK;
 }
 
@@ -268,19 +241,24 @@ namespace {
 // lse (stride lse_stride).
 mla_status_t combine_workspace(const mla_decode_plan_t* plan, void* out, mla_out_dtype_t out_dtype,
                                int64_t out_stride, float* lse, int64_t lse_stride, const void* workspace,
-                               size_t workspace_bytes, void* cuda_stream) {
+                               size_t workspace_bytes, void* cuda_stream, const float* out_scale = nullptr) {
   if (!plan_ok(plan) || !out || !workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
-  if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_FP32) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_FP32 &&
+      !(out_dtype == MLA_OUT_FP8_E4M3 && out_stride == MLA_KV_LORA_RANK))
+    return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
   if (plan->num_kv_splits == 1) return MLA_OK;
   DecodeParams p;
   memset(&p, 0, sizeof p);
   p.out = out;
   p.out_fp32 = out_dtype == MLA_OUT_FP32;
+  p.out_fp8 = out_dtype == MLA_OUT_FP8_E4M3;
+  p.out_scale = out_scale;
   p.out_stride = out_stride;
   p.lse = lse;
   p.lse_stride = lse_stride;
-  p.partials = reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(workspace)) + partials_offset(plan));
+  p.partials = reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(workspace)) +
+                                        MLA_WORKSPACE_HEADER_BYTES);
   p.batch = plan->batch;
   p.num_heads = plan->num_heads;
   p.q_len = plan->q_len;
@@ -322,7 +300,9 @@ mla_status_t mla_decode_shard(const mla_decode_plan_t* plan, const void* q_nope,
   p.lse_stride = kPartRow;
   p.kv_start = shard_start;
   p.total_lens = seq_lens;
-  return launch_fused(p, plan, (cudaStream_t)cuda_stream);
+  if (launch_split_kv(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return combine_workspace(plan, shard_partial, MLA_OUT_FP32, kPartRow, shard_partial + MLA_KV_LORA_RANK,
+                           kPartRow, workspace, workspace_bytes, cuda_stream);
 }
 
 mla_status_t mla_decode_fp8(const mla_decode_plan_t* plan, const void* q_nope, int64_t q_nope_row_stride,
@@ -339,7 +319,9 @@ mla_status_t mla_decode_fp8(const mla_decode_plan_t* plan, const void* q_nope, i
   if (st != MLA_OK) return st;
   p.q_scale = q_scale;
   p.out_scale = out_scale;
-  return launch_fused(p, plan, (cudaStream_t)cuda_stream);
+  if (launch_split_kv(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return combine_workspace(plan, out, out_dtype, MLA_KV_LORA_RANK, lse, 1, workspace, workspace_bytes, cuda_stream,
+                           out_scale);
 }
 
 mla_status_t mla_combine_shards(int64_t rows, int num_shards, const float* shard_partials, void* out,
@@ -370,12 +352,12 @@ mla_status_t mla_decode(const mla_decode_plan_t* plan, const void* q_nope, int64
                         const int32_t* seq_lens, float softmax_scale, const float* kv_scale,
                         void* out, mla_out_dtype_t out_dtype, float* lse, void* workspace,
                         size_t workspace_bytes, void* cuda_stream) {
-  DecodeParams p;
-  mla_status_t st = fill_params(plan, q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache,
-                                num_pages, block_table, block_table_stride, seq_lens, softmax_scale,
-                                kv_scale, out, out_dtype, lse, workspace, workspace_bytes, &p);
+  mla_status_t st = mla_split_kv(plan, q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache,
+                                 num_pages, block_table, block_table_stride, seq_lens,
+                                 softmax_scale, kv_scale, out, out_dtype, lse, workspace,
+                                 workspace_bytes, cuda_stream);
   if (st != MLA_OK) return st;
-  return launch_fused(p, plan, (cudaStream_t)cuda_stream);
+  return mla_combine(plan, out, out_dtype, lse, workspace, workspace_bytes, cuda_stream);
 }
 
 mla_status_t mla_decode_varlen(const mla_decode_plan_t* plan, const void* q_nope, int64_t q_nope_row_stride,
@@ -391,7 +373,8 @@ mla_status_t mla_decode_varlen(const mla_decode_plan_t* plan, const void* q_nope
                                 kv_scale, out, out_dtype, lse, workspace, workspace_bytes, &p);
   if (st != MLA_OK) return st;
   p.q_lens = q_lens;
-  return launch_fused(p, plan, (cudaStream_t)cuda_stream);
+  if (launch_split_kv(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return mla_combine(plan, out, out_dtype, lse, workspace, workspace_bytes, cuda_stream);
 }
 
 mla_status_t mla_decode_check_error(void* workspace, void* cuda_stream, int32_t info[4]) {

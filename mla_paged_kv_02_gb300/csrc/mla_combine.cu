@@ -23,14 +23,68 @@ namespace {
 
 constexpr int kWarps = 8;
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams p) {
+  const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (row >= (int64_t)p.batch * p.rows) return;
   const float* part = p.partials + row * p.part_row_stride;
-  // +inf in the first partial's LSE: the request had a single split and the
-  // split kernel wrote this row's out/lse itself.
-  if (__ldcg(part + kKvLora) == INFINITY) return;
-  merge_row(p, row, part, p.part_split_stride, p.splits, (p.out_fp8 && p.out_scale) ? *p.out_scale : 1.f);
+  const int64_t sstride = p.part_split_stride;
+
+  // Pass 1: the largest split LSE (NaN marks a request the split kernel rejected).
+  float M = -INFINITY;
+  bool nan_seen = false;
+  bool single = false;
+  for (int s = lane; s < p.splits; s += 32) {
+    const float v = part[(int64_t)s * sstride + kKvLora];
+    // +inf in the first partial's LSE: the request had a single split and the
+    // split kernel wrote this row's out/lse itself.
+    single |= (s == 0) & (v == INFINITY);
+    nan_seen |= (v != v);
+    M = fmaxf(M, v);
+  }
+  if (__any_sync(0xffffffffu, single)) return;
+  M = warp_max(M);
+  nan_seen = __any_sync(0xffffffffu, nan_seen);
+
+  float acc = 0.f;
+  for (int s = lane; s < p.splits; s += 32) {
+    const float v = part[(int64_t)s * sstride + kKvLora];
+    acc += (v == -INFINITY) ? 0.f : __expf(v - M);
+  }
+  acc = warp_sum(acc);
+  const float lse = (M == -INFINITY || nan_seen) ? (nan_seen ? NAN : -INFINITY) : M + logf(acc);
+
+  float o[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) o[k] = 0.f;
+  if (!nan_seen && M != -INFINITY) {
+    for (int s = 0; s < p.splits; ++s) {
+      const float* ps = part + (int64_t)s * sstride;
+      const float v = ps[kKvLora];
+      if (v == -INFINITY) continue;
+      const float w = __expf(v - lse);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) o[k] = fmaf(w, ps[lane + 32 * k], o[k]);
+    }
+  } else if (nan_seen) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o[k] = NAN;
+  }
+  const float osc = (p.out_fp8 && p.out_scale) ? *p.out_scale : 1.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) store_out(p, row, lane + 32 * k, o[k], osc);
+  if (p.lse && lane == 0) p.lse[row * p.lse_stride] = lse;
 }
 
 }  // namespace

@@ -169,8 +169,6 @@ struct Ctl {
   uint64_t drain;
   uint32_t tmem_base;
   int req;                     // the request this cluster works on
-  int merge;                   // this CTA arrived last: it merges the request's splits
-  int nsb;                     // splits the request uses
   int abort;
   int poisoned;
   float u_peer[2][kRows];      // [P buffer][row]: reference the peer computed its half with
@@ -361,9 +359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   // final out/lse itself; a split past the request's end only marks its
   // partial rows empty for the combine (their outputs are never read) and
   // leaves.  The combine applies the same rule.
-  const int nsb0 = request_splits(p, L);
-  if (threadIdx.x == 0) ctl->nsb = nsb0;
-  if (split >= nsb0) {
+  if (split >= request_splits(p, L)) {
     if (cta == 0 && (int)threadIdx.x < min(kRows, p.rows - row0))
       p.partials[(((int64_t)b * p.rows + row0 + threadIdx.x) * p.splits + split) * kPartRow + kKvLora] = -INFINITY;
     if (warp == 0) tmem_dealloc(ctl->tmem_base, kTmemCols);
@@ -1167,37 +1163,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
           if (rr < nr) dst[rr * kKvLora] = __float2bfloat16_rn(col[rr]);
       }
     }
-    // With the merge fused in, every thread that wrote partials fences them
-    // before the CTA reports its arrival.
-    if (p.fuse_merge && nsb > 1) __threadfence();
     tc_fence_before();
   }
   __syncthreads();
-  if (p.fuse_merge) {
-    // The last of the 2 * s_b CTAs of this (request, row group) to arrive
-    // merges the request's split partials for the group's rows: the combine
-    // done by the CTAs that finish last instead of a second kernel, reading
-    // partials that are still in L2.  (Request and split count come back from
-    // shared memory, so that they hold no register through the roles above.)
-    const int nsb = ctl->nsb;
-    if (nsb > 1) {
-      const int bm = ctl->req, rgm = blockIdx.x >> 1;
-      if (threadIdx.x == 0) {
-        const int old = atomicAdd(p.arrivals + (int64_t)bm * p.row_groups + rgm, 1);
-        __threadfence();
-        ctl->merge = old == 2 * nsb - 1;
-      }
-      __syncthreads();
-      if (ctl->merge) {
-        const float osc = (p.out_fp8 && p.out_scale) ? *p.out_scale : 1.f;
-        const int r0 = rgm * kRows;
-        const int rows_here = min(kRows, p.rows - r0);
-        const int64_t grow0 = (int64_t)bm * p.rows + r0;
-        for (int r = warp; r < rows_here; r += blockDim.x / 32)
-          merge_row(p, grow0 + r, p.partials + (grow0 + r) * p.splits * kPartRow, kPartRow, nsb, osc);
-      }
-    }
-  }
   if (threadIdx.x == 0 && *(volatile int*)&ctl->abort) {
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < kAbortSettleNs) {

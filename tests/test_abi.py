@@ -77,10 +77,7 @@ def test_plan_invariants(lib, B, H, q, L):
         rows = B * H * q
         want = rows * pl.num_kv_splits * 513 * 4 if pl.num_kv_splits > 1 else 0
         assert pl.partial_bytes == want
-        # header, then one arrival counter per (request, row group) rounded up
-        # to 256 bytes (only with more than one split), then the partials
-        arrivals = -(-B * pl.row_groups * 4 // 256) * 256 if pl.num_kv_splits > 1 else 0
-        assert pl.workspace_bytes == 256 + arrivals + want
+        assert pl.workspace_bytes == 256 + want
         # partials stay small next to the KV stream
         assert pl.partial_bytes <= 0.1 * B * L * 576 * 2 + 256 * 1024 * 1024
 

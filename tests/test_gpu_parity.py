@@ -239,47 +239,6 @@ def test_split_count_independence():
     assert max(float((o - outs[0]).abs().max()) for o in outs) <= 1e-3
 
 
-def test_fused_merge_equals_the_two_stage_path():
-    # mla_decode merges the splits in the split kernel (the last cluster of a
-    # request to finish); mla_split_kv + mla_combine keep the two stages.  Both
-    # merge the same partials with the same arithmetic, so they agree bitwise.
-    for q_len, lens, kw in ((4, [4, 500, 2000, 4096, 129], dict(sharp=5.0)), (2, [2, 70, 3000], dict(kv_fp8=True))):
-        inp = small(710 + q_len, q_len, lens, H=32, **kw)
-        dev = inp.to("cuda")
-        kvs = api.kv_scale_tensor(dev)
-        for s in (2, 5, 64):
-            pl = api.plan_for(dev, force_splits=s)
-            ws = api.alloc_workspace(pl, "cuda")
-            o1, l1 = api.alloc_outputs(dev, out_fp32=True)
-            o2, l2 = api.alloc_outputs(dev, out_fp32=True)
-            args = (dev.q_nope.view(-1, 512), dev.q_pe.view(-1, 64), dev.kv_cache, dev.block_table, dev.seq_lens,
-                    dev.softmax_scale, kvs)
-            assert _lib.decode(pl, *args, o1, l1, ws) == _lib.MLA_OK
-            assert _lib.split_kv(pl, *args, o2, l2, ws) == _lib.MLA_OK
-            assert _lib.combine(pl, o2, l2, ws) == _lib.MLA_OK
-            torch.cuda.synchronize()
-            assert _lib.check_error(ws)[0] == _lib.MLA_OK
-            assert torch.equal(o1, o2) and torch.equal(l1, l2), (q_len, s)
-
-
-def test_one_workspace_serves_plans_of_every_size():
-    # A workspace reserved once at the largest plan serves smaller plans with
-    # other split counts and batch sizes, in any order: the merge counters are
-    # zeroed on every call wherever the previous plan left partials.
-    big = small(720, 4, [4, 300, 1000, 4096, 2000, 77], H=32, sharp=4.0)
-    sub = synth.subset(big, [1, 3, 4])
-    dev_big, dev_sub = big.to("cuda"), sub.to("cuda")
-    ref_big, ref_sub = oracle.decode(big), oracle.decode(sub)
-    plans = [(dev_big, ref_big, 64), (dev_sub, ref_sub, 3), (dev_big, ref_big, 7), (dev_sub, ref_sub, 64),
-             (dev_big, ref_big, 2)]
-    ws = api.alloc_workspace(max((api.plan_for(d, force_splits=s) for d, _, s in plans),
-                                 key=lambda x: x.workspace_bytes), "cuda")
-    for d, (ro, rl), s in plans:
-        out, lse, pl = api.decode(d, force_splits=s, out_fp32=True, workspace=ws)
-        torch.cuda.synchronize()
-        compare(out, lse, ro, rl, what=f"reused workspace B={d.batch} splits={pl.num_kv_splits}")
-
-
 def test_mtp_rows_match_truncated_single_query_calls():
     q_len = 4
     inp = small(800, q_len, [4, 200, 777], H=32, sharp=4.0)
