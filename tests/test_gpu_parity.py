@@ -239,6 +239,23 @@ def test_split_count_independence():
     assert max(float((o - outs[0]).abs().max()) for o in outs) <= 1e-3
 
 
+def test_one_workspace_serves_plans_of_every_size():
+    # A workspace reserved once at the largest plan serves smaller plans with
+    # other split counts and batch sizes, in any order.
+    big = small(720, 4, [4, 300, 1000, 4096, 2000, 77], H=32, sharp=4.0)
+    sub = synth.subset(big, [1, 3, 4])
+    dev_big, dev_sub = big.to("cuda"), sub.to("cuda")
+    ref_big, ref_sub = oracle.decode(big), oracle.decode(sub)
+    plans = [(dev_big, ref_big, 64), (dev_sub, ref_sub, 3), (dev_big, ref_big, 7), (dev_sub, ref_sub, 64),
+             (dev_big, ref_big, 2)]
+    ws = api.alloc_workspace(max((api.plan_for(d, force_splits=s) for d, _, s in plans),
+                                 key=lambda x: x.workspace_bytes), "cuda")
+    for d, (ro, rl), s in plans:
+        out, lse, pl = api.decode(d, force_splits=s, out_fp32=True, workspace=ws)
+        torch.cuda.synchronize()
+        compare(out, lse, ro, rl, what=f"reused workspace B={d.batch} splits={pl.num_kv_splits}")
+
+
 def test_mtp_rows_match_truncated_single_query_calls():
     q_len = 4
     inp = small(800, q_len, [4, 200, 777], H=32, sharp=4.0)
