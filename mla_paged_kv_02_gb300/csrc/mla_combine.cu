@@ -34,12 +34,15 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// kGathered: shard partials [splits, rows, 513] read with the strides in p;
+// otherwise the workspace layout [rows, splits, 513] with constant strides.
+template <bool kGathered>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (row >= (int64_t)p.batch * p.rows) return;
-  const float* part = p.partials + row * p.part_row_stride;
-  const int64_t sstride = p.part_split_stride;
+  const float* part = p.partials + row * (kGathered ? p.part_row_stride : (int64_t)p.splits * kPartRow);
+  const int64_t sstride = kGathered ? p.part_split_stride : kPartRow;
 
   // Pass 1: the largest split LSE (NaN marks a request the split kernel rejected).
   float M = -INFINITY;
@@ -92,7 +95,10 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams
 cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.batch * p.rows;
   const unsigned blocks = (unsigned)((rows + kWarps - 1) / kWarps);
-  combine_kernel<<<blocks, kWarps * 32, 0, stream>>>(p);
+  if (p.part_split_stride == kPartRow && p.part_row_stride == (int64_t)p.splits * kPartRow)
+    combine_kernel<false><<<blocks, kWarps * 32, 0, stream>>>(p);
+  else
+    combine_kernel<true><<<blocks, kWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -218,10 +218,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
-// Splits request b uses: those whose chunk starts before its L tokens, at least
-// one and at most the plan's (the combine applies the same rule).
-__device__ __forceinline__ int request_splits(const DecodeParams& p, int L) {
-  return (int)max((int64_t)1, min((int64_t)p.splits, ((int64_t)L + p.chunk_tokens - 1) / p.chunk_tokens));
+// Request b uses the splits whose chunk starts before its L tokens, at least
+// one and at most the plan's: s_b = clamp(ceil(L / chunk), 1, splits).  The two
+// questions the kernel asks of s_b, without a division:
+//   does split s lie past the request's end (s >= s_b)?
+__device__ __forceinline__ bool split_past_end(const DecodeParams& p, int s, int L) {
+  return s > 0 && (int64_t)s * p.chunk_tokens >= L;
+}
+//   does the request use a single split (s_b == 1)?
+__device__ __forceinline__ bool single_split(const DecodeParams& p, int L) {
+  return p.splits == 1 || L <= p.chunk_tokens;
 }
 
 // Bounded wait that also gives up once any role of this CTA has aborted.  CTA
@@ -359,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   // final out/lse itself; a split past the request's end only marks its
   // partial rows empty for the combine (their outputs are never read) and
   // leaves.  The combine applies the same rule.
-  if (split >= request_splits(p, L)) {
+  if (split_past_end(p, split, L)) {
     if (cta == 0 && (int)threadIdx.x < min(kRows, p.rows - row0))
       p.partials[(((int64_t)b * p.rows + row0 + threadIdx.x) * p.splits + split) * kPartRow + kKvLora] = -INFINITY;
     if (warp == 0) tmem_dealloc(ctl->tmem_base, kTmemCols);
@@ -1075,10 +1081,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     const bool has = l_tot > 0.f;
     const float il = has ? kv_scale / l_tot : 0.f;
     const int64_t grow0 = (int64_t)b * p.rows + row0;
-    const int nsb = request_splits(p, L);
+    const bool one_split = single_split(p, L);
     if (cta == 0 && row_ok) {
       const float lv = bad ? NAN : (has ? (r_ref + lg2(l_tot)) * kLn2 : -INFINITY);
-      if (nsb == 1) {
+      if (one_split) {
         if (p.lse) p.lse[(grow0 + r) * p.lse_stride] = lv;
         // +inf (never a real LSE) in split 0's slot: the combine leaves the row alone
         if (p.splits > 1) p.partials[(grow0 + r) * p.splits * kPartRow + kKvLora] = INFINITY;
@@ -1134,7 +1140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       __syncwarp();  // the tile may be rewritten once every lane holds its column
       const int dim = (int)cta * 256 + c0 + lane;
       const int nr = min(32, rows_here - quad * 32);  // rows of this warp that exist
-      if (nsb > 1) {
+      if (!one_split) {
         float* dst = p.partials + ((grow0 + quad * 32) * p.splits + split) * kPartRow + dim;
         const int64_t step = (int64_t)p.splits * kPartRow;
 #pragma unroll
