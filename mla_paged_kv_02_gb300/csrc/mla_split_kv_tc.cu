@@ -153,7 +153,6 @@ struct Ctl {
   uint64_t q_full;
   uint64_t raw_full[kMaxStages];
   uint64_t full[kMaxStages];
-  uint64_t half_ready[kMaxStages][2];  // FP8 cache, bf16 query: bf16 c_kv chunks 0-1 / chunks 2-3 and k_pe converted
   uint64_t empty[kMaxStages];     // this CTA's PV of the stage's page has completed
   uint64_t q_tmem;             // Q moved from shared to tensor memory (count 4)
   uint64_t s_full[2];          // QK^T of the page is in TMEM
@@ -201,12 +200,6 @@ __device__ __forceinline__ bool wg_sync_or(bool v) {
   return r != 0;
 }
 __device__ __forceinline__ void conv_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
-// Barrier 3 of the converter group: "every thread holds its e4m3 bytes".  The
-// warps that overwrite e4m3 bytes wait on it; the others only arrive.  It is a
-// barrier of its own, never mixed with barrier 2's reductions, and the full
-// reduction at the top of every iteration keeps any warp from lapping it.
-__device__ __forceinline__ void conv_held_wait() { asm volatile("bar.sync 3, 128;" ::: "memory"); }
-__device__ __forceinline__ void conv_held_arrive() { asm volatile("bar.arrive 3, 128;" ::: "memory"); }
 __device__ __forceinline__ bool conv_sync_or(bool v) {
   uint32_t r;
   asm volatile(
@@ -300,11 +293,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     mbar_init(&ctl->q_full, 1);
     for (int s = 0; s < kNS; ++s) {
       mbar_init(&ctl->raw_full[s], 1);
-      mbar_init(&ctl->full[s], kFp8 ? 4 : 1);  // TMA landing (bf16) / FP8-query converter warps
+      mbar_init(&ctl->full[s], kFp8 ? 4 : 1);
       mbar_init(&ctl->empty[s], 1);
       mbar_init(&ctl->qk_done[s], 1);
-      mbar_init(&ctl->half_ready[s][0], 2);  // two converter warps each
-      mbar_init(&ctl->half_ready[s][1], 2);
     }
     mbar_init(&ctl->q_tmem, 4);
     mbar_init(&ctl->s_full[0], 1);
@@ -524,29 +515,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       const uint64_t qpe_desc = sdesc_sw64(smem_u32(sQpe), 16, 512);
       bool ok = wait_bar(ctl, &ctl->q_tmem, 0, p, 2);
       for (int j = 0; ok && j < n_pages; ++j) {
-        // bf16 cache: the page has landed.  FP8 cache: its first two c_kv
-        // chunks are converted (the rest is waited for below).
-        const uint32_t ph = (j / kNS) & 1;
-        if (!wait_bar(ctl, kFp8 ? &ctl->half_ready[j % kNS][0] : &ctl->full[j % kNS], ph, p, 3) ||
+        if (!wait_bar(ctl, &ctl->full[j % kNS], (j / kNS) & 1, p, 3) ||
             !wait_bar(ctl, &ctl->s_free[j & 1], ((j >> 1) & 1) ^ 1, p, 4))
           break;
         tc_fence_after();
         const uint64_t k_desc = sdesc_sw128(kv_addr + (j % kNS) * kStageBytes, 16, 1024);
         const uint32_t d = tmem + kColS + (j & 1) * 64;
         for (int k = 0; k < 4; ++k) {
-          if (kFp8 && k == 2) {  // chunks 2-3 and k_pe of an FP8 page
-            if (!wait_bar(ctl, &ctl->half_ready[j % kNS][1], ph, p, 26)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // A = Q chunk k from TMEM: 16 k per MMA = 8 columns
             mma_bf16_ts(d, tmem + kColQ + k * 32 + kk * 8, k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4),
                         kIdescQK, (k | kk) ? 1u : 0u);
         }
-        if (!ok) break;
         {  // this CTA's 32 k_pe columns: two K-steps along 64-byte swizzled rows
           const uint64_t kpe_desc = sdesc_sw64(kv_addr + (j % kNS) * kStageBytes + 4 * kKvChunkBytes, 16, 512);
 #pragma unroll
@@ -652,17 +632,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     }
   } else if (kFp8 && !kQ8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
     // ------------------------------------------------------------ e4m3 -> bf16 converter
-    // Two halves, so that QK can start on the first while the second converts:
-    // warps 0-1 of the group convert c_kv chunks 0 and 1 of token ct (64 e4m3
-    // bytes each, into 128-byte swizzled bf16 rows), whose bf16 tiles do not
-    // overlap the e4m3 bytes, and release them at once (`half_ready[s][0]`);
-    // warps 2-3 convert chunks 2 and 3 and the 32 k_pe bytes of token ct-64
-    // (k_pe into 64-byte swizzled rows), whose tiles cover the e4m3 bytes, so
-    // they first wait until every thread of the group holds its bytes, then
-    // release `half_ready[s][1]`.  Lane t reads the 16-byte units of its row
-    // starting at unit t%4, which spreads a warp's reads over the banks.
+    // Thread ct converts tokens ct/2 of chunks 2(ct%2) and 2(ct%2)+1 (64 e4m3
+    // bytes each, into 128-byte swizzled bf16 rows), and threads below 64 also
+    // token ct's 32 k_pe bytes (into 64-byte swizzled rows).
     const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
-    const int t_c = ct & 63, h = ct >> 6;
+    const int t_c = ct >> 1, c0 = 2 * (ct & 1);
     for (int j = 0; j < n_pages; ++j) {
       const int s = j % kNS;
       if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[s], (j / kNS) & 1, p, 9))) break;
@@ -670,53 +644,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       uint4 raw[2][4], rpe[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const uint4* src = reinterpret_cast<const uint4*>(stage + Lay::kRawOff + (2 * h + k) * kRawBox + t_c * 64);
+        const uint4* src = reinterpret_cast<const uint4*>(stage + Lay::kRawOff + (c0 + k) * kRawBox + t_c * 64);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) raw[k][q] = src[(q + t_c) & 3];
+        for (int q = 0; q < 4; ++q) raw[k][q] = src[q];
       }
-      if (h == 1) {
-        const uint4* src = reinterpret_cast<const uint4*>(stage + Lay::kRawPeOff + t_c * 32);
+      if (ct < 64) {
+        const uint4* src = reinterpret_cast<const uint4*>(stage + Lay::kRawPeOff + ct * 32);
         rpe[0] = src[0];
         rpe[1] = src[1];
       }
-      // Chunks 2-3 and k_pe overwrite e4m3 bytes: every thread must hold its
-      // bytes first.  Chunks 0-1 do not: their warps only signal.
-      if (h == 1) conv_held_wait(); else conv_held_arrive();
+      conv_sync();  // every raw byte is in registers before the bf16 writes overlap them
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        uint8_t* dst = stage + (2 * h + k) * kKvChunkBytes + t_c * 128;
+        uint8_t* dst = stage + (c0 + k) * kKvChunkBytes + t_c * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int u = (q + t_c) & 3;  // the 16-byte unit raw[k][q] holds
           const uint32_t w[4] = {raw[k][q].x, raw[k][q].y, raw[k][q].z, raw[k][q].w};
           uint32_t o[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            o[2 * e] = e4m3x2_to_bf16x2((uint16_t)(w[e] & 0xFFFFu));
-            o[2 * e + 1] = e4m3x2_to_bf16x2((uint16_t)(w[e] >> 16));
+          for (int h = 0; h < 4; ++h) {
+            o[2 * h] = e4m3x2_to_bf16x2((uint16_t)(w[h] & 0xFFFFu));
+            o[2 * h + 1] = e4m3x2_to_bf16x2((uint16_t)(w[h] >> 16));
           }
-          *reinterpret_cast<uint4*>(dst + (((2 * u) ^ (t_c & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(dst + (((2 * u + 1) ^ (t_c & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          *reinterpret_cast<uint4*>(dst + (((2 * q) ^ (t_c & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ (t_c & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
       }
-      if (h == 1) {
-        uint8_t* dst = stage + 4 * kKvChunkBytes + t_c * 64;
+      if (ct < 64) {
+        uint8_t* dst = stage + 4 * kKvChunkBytes + ct * 64;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const uint32_t w[4] = {rpe[q].x, rpe[q].y, rpe[q].z, rpe[q].w};
           uint32_t o[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            o[2 * e] = e4m3x2_to_bf16x2((uint16_t)(w[e] & 0xFFFFu));
-            o[2 * e + 1] = e4m3x2_to_bf16x2((uint16_t)(w[e] >> 16));
+          for (int h = 0; h < 4; ++h) {
+            o[2 * h] = e4m3x2_to_bf16x2((uint16_t)(w[h] & 0xFFFFu));
+            o[2 * h + 1] = e4m3x2_to_bf16x2((uint16_t)(w[h] >> 16));
           }
-          *reinterpret_cast<uint4*>(dst + (((2 * q) ^ ((t_c >> 1) & 3)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ ((t_c >> 1) & 3)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          *reinterpret_cast<uint4*>(dst + (((2 * q) ^ ((ct >> 1) & 3)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ ((ct >> 1) & 3)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
       }
       fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->half_ready[s][h]);
+      conv_sync();
+      if (lane == 0) mbar_arrive(&ctl->full[s]);
     }
   } else if (warp >= send_warp0<kFp8>() && warp < send_warp0<kFp8>() + 4) {
     // ------------------------------------------------------------ S sender
