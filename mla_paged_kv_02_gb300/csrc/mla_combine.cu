@@ -43,8 +43,54 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams
   if (row >= (int64_t)p.batch * p.rows) return;
   const float* part = p.partials + row * (kGathered ? p.part_row_stride : (int64_t)p.splits * kPartRow);
   const int64_t sstride = kGathered ? p.part_split_stride : kPartRow;
+  const float osc = (p.out_fp8 && p.out_scale) ? *p.out_scale : 1.f;
 
-  // Pass 1: the largest split LSE (NaN marks a request the split kernel rejected).
+  if (p.splits <= 32) {
+    // Lane s holds split s's LSE and, once the total is known, its weight.
+    // The outputs of four splits are loaded at a time (64 loads per lane in
+    // flight, the weights by shuffle), so a row costs one dependent round trip
+    // per four splits instead of two per split.
+    const float lv = lane < p.splits ? part[(int64_t)lane * sstride + kKvLora] : -INFINITY;
+    // +inf in the first partial's LSE: the request had a single split and the
+    // split kernel wrote this row's out/lse itself.
+    if (__shfl_sync(0xffffffffu, lv, 0) == INFINITY) return;
+    const bool nan_seen = __any_sync(0xffffffffu, lv != lv);
+    const float M = warp_max(lv);
+    const float acc = warp_sum(lv == -INFINITY ? 0.f : __expf(lv - M));
+    const float lse = (M == -INFINITY || nan_seen) ? (nan_seen ? NAN : -INFINITY) : M + logf(acc);
+    const float wl = (lv == -INFINITY || nan_seen || M == -INFINITY) ? 0.f : __expf(lv - lse);
+    float o[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o[k] = nan_seen ? NAN : 0.f;
+    if (!nan_seen) {
+      for (int s0 = 0; s0 < p.splits; s0 += 4) {
+        float w[4], v[4][16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = __shfl_sync(0xffffffffu, wl, (s0 + j) & 31);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // Splits past the last, and empty ones (weight 0, outputs not read).
+          const bool use = s0 + j < p.splits && w[j] != 0.f;
+          const float* ps = part + (int64_t)(s0 + j) * sstride + lane;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[j][k] = use ? ps[32 * k] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float wj = s0 + j < p.splits ? w[j] : 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) o[k] = fmaf(wj, v[j][k], o[k]);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) store_out(p, row, lane + 32 * k, o[k], osc);
+    if (p.lse && lane == 0) p.lse[row * p.lse_stride] = lse;
+    return;
+  }
+
+  // More than 32 splits.  Pass 1: the largest split LSE (NaN marks a request
+  // the split kernel rejected).
   float M = -INFINITY;
   bool nan_seen = false;
   bool single = false;
@@ -84,7 +130,6 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const DecodeParams
 #pragma unroll
     for (int k = 0; k < 16; ++k) o[k] = NAN;
   }
-  const float osc = (p.out_fp8 && p.out_scale) ? *p.out_scale : 1.f;
 #pragma unroll
   for (int k = 0; k < 16; ++k) store_out(p, row, lane + 32 * k, o[k], osc);
   if (p.lse && lane == 0) p.lse[row * p.lse_stride] = lse;
