@@ -458,9 +458,14 @@ def main():
         "tflops": aflops * world / (step_us * 1e-6) / 1e12,
         "kernel_us": ({"split_kv+combine": split_us} if q8 else {"split_kv": split_us, "combine": comb_us}),
         "roofline": roofline,
-        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "mode": "copies on a second stream, overlapping the neighbouring steps' decodes",
-                "serial_value": e2e_serial_us},
+        # The faster of the two ways a caller can drive the same copies and
+        # decodes (overlapped wins except for launch-bound tiny steps, where
+        # the cross-stream waits cost more than they hide); both are reported.
+        "e2e": {"value": min(e2e_us, e2e_serial_us), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "mode": ("copies on a second stream, overlapping the neighbouring steps' decodes"
+                         if e2e_us <= e2e_serial_us else "one stream: copy in, decode, copy out"),
+                "pipelined_value": e2e_us, "serial_value": e2e_serial_us},
         "gpu_launches": args.steps * (1 + (pl.num_kv_splits > 1)),
         "clocks": clk,
     }
