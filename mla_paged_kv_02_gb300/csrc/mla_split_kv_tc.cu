@@ -156,13 +156,13 @@ struct Ctl {
   uint64_t empty[kMaxStages];     // this CTA's PV of the stage's page has completed
   uint64_t q_tmem;             // Q moved from shared to tensor memory (count 4)
   uint64_t s_full[2];          // QK^T of the page is in TMEM
-  uint64_t s_free[2];          // the 4 softmax warps have read it (count 4)
+  uint64_t s_free[2];          // the live softmax and sender warps have read it (count 2 x live quadrants)
   uint64_t sin_full[4];        // per quadrant: the peer's partial S landed (count 1 + 4 KB of st.async bytes)
   uint64_t sin_free[4];        // per quadrant: the peer consumed what this CTA sent (count 1, remote)
   uint64_t p_free[2];          // PV done in both CTAs: that P buffer rewritable (count 2)
-  uint64_t pv_ready[2];        // local P halves written (count 4) + the peer's halves landed
-  uint64_t u_ready[2];         // the peer's references for the page landed (count 4 + 512 B)
-  uint64_t checked[2];         // the 4 local warps ran the page's reference check (count 4)
+  uint64_t pv_ready[2];        // local P halves written (count: live quadrants) + the peer's halves landed
+  uint64_t u_ready[2];         // the peer's references for the page landed (count: live quadrants + 128 B each)
+  uint64_t checked[2];         // the live local warps ran the page's reference check (count: live quadrants)
   uint64_t p_recv[4];          // per quadrant: the peer holds this CTA's P rows it had to scale (count 1, remote)
   uint64_t qk_done[kMaxStages];  // FP8 query: QK^T of the stage's page completed (its e4m3 bytes are free)
   uint64_t fin;                // the peer's row sums delivered (count 4 + 512 B)
@@ -239,6 +239,16 @@ __device__ __forceinline__ int request_splits(const DecodeParams& p, int L) {
   return (int)max((int64_t)1, min((int64_t)p.splits, ((int64_t)L + p.chunk_tokens - 1) / p.chunk_tokens));
 }
 
+// TMEM lane quadrants holding at least one query row of the cluster's row
+// group.  With fewer than 128 rows (few heads, short MTP) the softmax and
+// sender warps of the other quadrants take no part in the page loop: their
+// rows are never written, so their scores and P are neither exchanged nor
+// computed, which cuts the pair's per-page traffic by the same factor.
+// Recomputed where needed rather than kept in a register across the kernel.
+__device__ __forceinline__ int live_quads(const DecodeParams& p) {
+  return min(4, (min(kRows, p.rows - (int)(blockIdx.x >> 1) * kRows) + 31) >> 5);
+}
+
 // Bounded wait that also gives up once any role of this CTA has aborted.  CTA
 // scope suffices for every barrier completed by local arrives, by transaction
 // bytes (TMA, st.async, bulk copies) or by a relaxed "consumed" signal; only a
@@ -299,6 +309,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
   const int nb4 = (p.batch + 3) >> 2;  // lengths padded with INT_MIN, which never outranks anything
   const int my_len = (lpt && (int)threadIdx.x < p.batch) ? p.seq_lens[threadIdx.x] : INT_MIN;
   if (threadIdx.x == 0) {
+    const int nq = live_quads(p);
     mbar_init(&ctl->q_full, 1);
     for (int s = 0; s < kNS; ++s) {
       mbar_init(&ctl->raw_full[s], 1);
@@ -309,17 +320,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     mbar_init(&ctl->q_tmem, 4);
     mbar_init(&ctl->s_full[0], 1);
     mbar_init(&ctl->s_full[1], 1);
-    mbar_init(&ctl->s_free[0], 8);  // softmax and sender warps
-    mbar_init(&ctl->s_free[1], 8);
+    mbar_init(&ctl->s_free[0], 2 * nq);  // live softmax and sender warps
+    mbar_init(&ctl->s_free[1], 2 * nq);
     for (int q = 0; q < 4; ++q) {
       mbar_init(&ctl->sin_full[q], 1);
       mbar_init(&ctl->sin_free[q], 1);
       mbar_init(&ctl->p_recv[q], 1);
     }
     for (int e = 0; e < 2; ++e) {
-      mbar_init(&ctl->pv_ready[e], 4);
-      mbar_init(&ctl->checked[e], 4);
-      mbar_init(&ctl->u_ready[e], 4);
+      mbar_init(&ctl->pv_ready[e], nq);
+      mbar_init(&ctl->checked[e], nq);
+      mbar_init(&ctl->u_ready[e], nq);
     }
     mbar_init(&ctl->p_free[0], 2);
     mbar_init(&ctl->p_free[1], 2);
@@ -712,7 +723,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     uint8_t* sout_row = sout_quad + lane * 128;
     const uint32_t sin_quad_peer = mapa_shared(smem_u32(sSin + quad * kSinQuadBytes), peer);
     const uint32_t sin_full_peer = mapa_shared(smem_u32(&ctl->sin_full[quad]), peer);
-    for (int j = 0; j < n_pages; ++j) {
+    const int n_send = quad < live_quads(p) ? n_pages : 0;
+    for (int j = 0; j < n_send; ++j) {
       const int sb = j & 1;
       if (!__all_sync(0xffffffffu, wait_bar(ctl, &ctl->s_full[sb], (j >> 1) & 1, p, 20))) break;
       tc_fence_after();
@@ -916,8 +928,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     // the same iteration would stall every page for a full memory latency.
     int page_next = n_pages > 0 ? bt_row[0] : 0;
     float sv_next[32];
-    if (ok && n_pages > 0 && !take_s(0, sv_next)) ok = false;
-    for (int j = 0; ok && j < n_pages; ++j) {
+    const bool live = quad < live_quads(p);  // (the group's other warps go straight to the epilogue)
+    if (ok && live && n_pages > 0 && !take_s(0, sv_next)) ok = false;
+    for (int j = 0; ok && live && j < n_pages; ++j) {
       const int e = j & 1;   // pv_ready / checked / peer references of this page
       const int tok0 = lo + j * kPage;  // lo is page aligned
       const int page = page_next;
@@ -990,16 +1003,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
 
 
       // V rows of tokens at or past L (or of a page that was never loaded) may
-      // hold anything, NaN included; zero this CTA's 256 V columns of them.
-      // Thread t of the group clears half of token row t/2.
+      // hold anything, NaN included; zero this CTA's 256 V columns of them (64
+      // tokens x four 128-byte chunk rows, shared among the live warps' threads).
       const int n_valid = page_ok ? min(L - tok0, kPage) : 0;
       if (!kQ8 && n_valid < kPage) {  // (with an FP8 query the converter writes those rows as zeros)
-        const int t = r >> 1;
-        if (t >= n_valid) {
-          uint8_t* stage = sKV + (j % kNS) * kStageBytes;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint4* rowp = reinterpret_cast<uint4*>(stage + ((r & 1) * 2 + c) * kKvChunkBytes + t * 128);
+        uint8_t* stage = sKV + (j % kNS) * kStageBytes;
+        const int step = 32 * live_quads(p);
+        for (int i = r; i < kPage * 4; i += step) {
+          const int t = i >> 2;
+          if (t >= n_valid) {
+            uint4* rowp = reinterpret_cast<uint4*>(stage + (i & 3) * kKvChunkBytes + t * 128);
 #pragma unroll
             for (int u = 0; u < 8; ++u) rowp[u] = make_uint4(0, 0, 0, 0);
           }
