@@ -130,7 +130,12 @@ mla_status_t mla_workspace_init(void* workspace, size_t workspace_bytes, void* c
  *   seq_lens: int32 [batch] on the device, q_len <= L_b <= plan->max_seq_len
  *   softmax_scale : multiplies q.x (1/sqrt(192) for DeepSeek-R1); read per call
  *   kv_scale: device fp32 dequant scale for an FP8 cache (NULL = 1.0); read by
- *             the kernel on every launch, never cached
+ *             the kernel on every launch, never cached.  With an FP8 cache the
+ *             tensor-core operands are f16 (every e4m3 value is exact in f16,
+ *             and the conversion is one instruction per pair), so the bf16
+ *             query must lie within +-65504: a value beyond that is a
+ *             device-side input error (index -4, value = the row i*H + h within
+ *             the request) and that row alone is written as NaN
  *   out     : [batch, q_len, H, 512] bf16 or fp32 (out_dtype)
  *   lse     : [batch, q_len, H] fp32 natural-log LSE, or NULL
  *   workspace, workspace_bytes : >= plan->workspace_bytes, 256-byte aligned;

@@ -73,13 +73,12 @@ constexpr int kPBytes = kRows * 128;    // P[128 rows x 64 tokens] bf16
 constexpr int kPHalfBytes = kPBytes / 2;  // one token half of P
 constexpr int kStageOff = 0;
 constexpr int kCtlBytes = 2048;
-constexpr int kRawBox = 64 * 64;          // FP8: one 64 tokens x 64 bytes box of e4m3 c_kv
-constexpr int kRawPeBox = 64 * 32;        // FP8: 64 tokens x 32 bytes of e4m3 k_pe
 
 // Shared-memory layout.  Each CTA holds four c_kv chunks and half of k_pe (32
-// columns, 64-byte swizzled rows) of every page in bf16, so QK^T is 18 MMAs in
-// both CTAs.  With an FP8 cache the e4m3 bytes land in the upper half of the
-// stage and the converter writes the bf16 tiles over the whole stage.
+// columns, 64-byte swizzled rows) of every page in bf16 (f16 with an FP8
+// cache), so QK^T is 18 MMAs in both CTAs.  With an FP8 cache the e4m3 codes
+// land at stage + 16 KB (below) and the converter writes the f16 tiles over
+// the whole stage.
 template <bool kFp8>
 struct Layout {
   static constexpr int kStageBytes = 4 * kKvChunkBytes + kPeHalfBytes;
@@ -94,22 +93,20 @@ struct Layout {
   static constexpr int kQpeBytes = kQChunkBytes / 2;
   static constexpr int kCtlOff = kQpeOff + kQpeBytes;
   static constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;    // + alignment slack
-  static constexpr int kRawOff = kStageBytes / 2;                    // FP8: e4m3 columns in the upper half of a stage
-  static constexpr int kRawPeOff = kRawOff + 4 * kRawBox;            // FP8: the 32 e4m3 k_pe columns
   static_assert(4 * kQChunkBytes <= 2 * kStageBytes, "Q staging");
   static_assert(kStages >= 3 && kStages <= kMaxStages, "stages");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kStageBytes % 1024 == 0 && kPOff % 1024 == 0 && kQpeOff % 1024 == 0, "swizzle atoms");
 };
 
-// FP8 query (kQ8, FP8 cache): QK^T runs on the e4m3 codes themselves
-// (tcgen05 kind::f8f6f4).  The CTA's 256 e4m3 c_kv columns of a page land
-// 128B-swizzled as two 8 KB boxes at stage + 16 KB, the space of bf16 V chunks 2
-// and 3, which the converter writes only once QK of the page has completed; its
-// 32 e4m3 k_pe columns land 32B-swizzled at stage + 32 KB and are never
-// overwritten (k_pe needs no bf16 copy: it only enters QK).  The query's c_kv
-// columns sit in tensor memory four codes per column, its 32 q_pe codes per row
-// in shared memory (32B swizzle).
+// FP8 cache: the CTA's 256 e4m3 c_kv columns of a page land 128B-swizzled as
+// two 8 KB boxes at stage + 16 KB, the space of f16 chunks 2 and 3, and its 32
+// e4m3 k_pe columns 32B-swizzled at stage + 32 KB, under the f16 k_pe tile.
+// FP8 query (kQ8): QK^T runs on those codes themselves (tcgen05 kind::f8f6f4),
+// so the converter writes chunks 2-3 only once QK of the page has completed and
+// never touches the k_pe codes (k_pe only enters QK).  The query's c_kv columns
+// sit in tensor memory four codes per column, its 32 q_pe codes per row in
+// shared memory (32B swizzle).
 constexpr int kQ8RawOff = 16 * 1024;
 constexpr int kQ8RawPeOff = 32 * 1024;
 constexpr int kQ8Box = 64 * 128;     // 64 tokens x 128 e4m3 columns
@@ -142,6 +139,14 @@ constexpr uint64_t kAbortSettleNs = 200000ull;
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdescQK8 = idesc_e4m3(128, 64);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
+// FP8 cache: an e4m3 pair widens to f16 in one conversion (to bf16 it takes
+// four), so the FP8-cache instances run their bf16-shaped MMAs on f16 operands:
+// the cache's codes, P, and (with a bf16 query) Q and q_pe converted once per
+// cluster.  Every e4m3 value is exact in f16, P (at most 2^8) gains three
+// mantissa bits, and a bf16 query is exact in f16 within +-65504 (beyond that
+// the request is reported as an input error).  A and B always share the type.
+constexpr uint32_t kIdescQKh = idesc_f16(128, 64, false, false);
+constexpr uint32_t kIdescPVh = idesc_f16(128, 256, false, true);
 
 // Bytes the peer's warp of a quadrant delivers per page: its 32 rows' P halves
 // (64 B each) into pv_ready, and the references they are computed with (4 B
@@ -210,12 +215,50 @@ __device__ __forceinline__ bool conv_sync_or(bool v) {
   return r != 0;
 }
 
-// Two e4m3 codes (low byte first) -> two bf16 values, exactly.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
+// Two e4m3 codes (low byte first) -> two f16 values, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-  __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-  return *reinterpret_cast<uint32_t*>(&b);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// Two floats -> the MMA operand pair: bf16 (bf16 cache) or f16 (FP8 cache).
+template <bool kHalf>
+__device__ __forceinline__ uint32_t pack_pair(float a, float b) {
+  if constexpr (kHalf) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+template <bool kHalf>
+__device__ __forceinline__ float2 unpack_pair(uint32_t w) {
+  if constexpr (kHalf)
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  else
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+
+// A P pair times a power of two f <= 1 (f16: in half precision, where an f
+// below the smallest subnormal rounds to 0 like the products it would give).
+template <bool kHalf>
+__device__ __forceinline__ uint32_t scale_pair(uint32_t w, float f) {
+  if constexpr (kHalf) {
+    __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&w), __float2half2_rn(f));
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    const float2 x = unpack_pair<false>(w);
+    return pack_pair<false>(x.x * f, x.y * f);
+  }
+}
+
+// A bf16 pair -> an f16 pair (exact within +-65504; `big` is set for a value
+// that would round to infinity).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& big) {
+  const float a = __uint_as_float(w << 16), b = __uint_as_float(w & 0xFFFF0000u);
+  big |= fabsf(a) >= 65520.f || fabsf(b) >= 65520.f;
+  return pack_pair<true>(a, b);
 }
 
 // Request b uses the splits whose chunk starts before its L tokens, at least
@@ -462,16 +505,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         if (page < 0 || page >= p.num_pages) {
           if (cta == 0) report_error(p.err, MLA_ERR_DEVICE_INPUT, b, first_page + j, page);
           mbar_arrive(land);  // nothing to load; consumers mask the whole page
-        } else if (kQ8) {  // e4m3 for QK^T as it is: two 128B-swizzled c_kv boxes, one k_pe box
+        } else if (kFp8) {  // e4m3: two 128B-swizzled boxes of 128 c_kv codes, one 32B-swizzled k_pe box
           mbar_arrive_expect_tx(land, 2 * kQ8Box + kQ8PeBox);
           for (int k = 0; k < 2; ++k)
             tma_load_2d(stage + kQ8RawOff + k * kQ8Box, &tm_kv, land, 256 * (int)cta + 128 * k, page * kPage);
           tma_load_2d(stage + kQ8RawPeOff, &tm_kpe, land, 8 * 64 + 32 * (int)cta, page * kPage);
-        } else if (kFp8) {  // e4m3: the CTA's four c_kv chunks and 32 k_pe columns
-          mbar_arrive_expect_tx(land, 4 * kRawBox + kRawPeBox);
-          for (int k = 0; k < 4; ++k)
-            tma_load_2d(stage + Lay::kRawOff + k * kRawBox, &tm_kv, land, (g0 + k) * 64, page * kPage);
-          tma_load_2d(stage + Lay::kRawPeOff, &tm_kpe, land, 8 * 64 + 32 * (int)cta, page * kPage);
         } else {
           // The CTA's four c_kv chunks in one 3-D box (columns x rows x chunks),
           // which lands as [chunk][row][128 B], and its 32 k_pe columns in a 2-D
@@ -544,14 +582,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         for (int k = 0; k < 4; ++k) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // A = Q chunk k from TMEM: 16 k per MMA = 8 columns
-            mma_bf16_ts(d, tmem + kColQ + k * 32 + kk * 8, k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4),
-                        kIdescQK, (k | kk) ? 1u : 0u);
+            mma_16b_ts(d, tmem + kColQ + k * 32 + kk * 8, k_desc + (uint64_t)((k * kKvChunkBytes + kk * 32) >> 4),
+                        kFp8 ? kIdescQKh : kIdescQK, (k | kk) ? 1u : 0u);
         }
         {  // this CTA's 32 k_pe columns: two K-steps along 64-byte swizzled rows
           const uint64_t kpe_desc = sdesc_sw64(kv_addr + (j % kNS) * kStageBytes + 4 * kKvChunkBytes, 16, 512);
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
-            mma_bf16_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4), kpe_desc + (uint64_t)((kk * 32) >> 4), kIdescQK, 1u);
+            mma_16b_ss(d, qpe_desc + (uint64_t)((kk * 32) >> 4), kpe_desc + (uint64_t)((kk * 32) >> 4),
+                       kFp8 ? kIdescQKh : kIdescQK, 1u);
         }
         mma_commit(&ctl->s_full[j & 1]);
       }
@@ -590,9 +629,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
 #pragma unroll
           for (int t = 0; t < 2; ++t) {  // A = P tokens 16kk..16kk+15: two 8-token chunks of half h
             const int kk = 2 * h + t;
-            mma_bf16_ss(tmem + kColO,
+            mma_16b_ss(tmem + kColO,
                         sdesc_noswz(p_addr + pb * kPBytes + h * kPHalfBytes + ((2 * kk) & 3) * 128, 128, 512),
-                        v_desc + (uint64_t)((kk * 2048) >> 4), kIdescPV, (j > 0 || i > 0 || t > 0) ? 1u : 0u);
+                        v_desc + (uint64_t)((kk * 2048) >> 4), kFp8 ? kIdescPVh : kIdescPV,
+                        (j > 0 || i > 0 || t > 0) ? 1u : 0u);
           }
         }
         if (!ok) break;
@@ -604,32 +644,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
       while (!mbar_try_wait(smem_u32(&ctl->drain), 0))
         if (globaltimer_ns() - t0 > kWaitLimitNs) break;
     }
-  } else if (kQ8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
-    // ------------------------------------------------------------ e4m3 -> bf16 V (FP8 query)
-    // Warps 0-1 of the group convert c_kv box 0 and warps 2-3 box 1: thread ct
-    // takes token ct%64 (128 codes, 128B-swizzled) into bf16 V chunks 2h and
-    // 2h+1 (h = ct/64), writing zeros for tokens at or past L and for a page
-    // that was never loaded (such slots may hold anything).  Box 1's bf16
-    // output covers the codes QK reads, so its warps first wait for QK of the
-    // page to complete.  One copy of the conversion code serves both boxes.
+  } else if (kFp8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
+    // ------------------------------------------------------------ e4m3 -> f16 converter
+    // The CTA's 256 c_kv codes of a page land as two 128B-swizzled boxes of 128
+    // codes at stage + 16 KB.  Thread ct takes token t = ct%64 of box h = ct/64
+    // (eight 16-byte units) into f16 chunks 2h and 2h+1 (128B swizzle): a warp's
+    // loads and stores cover eight distinct units per eight lanes, free of bank
+    // conflicts.  Box 1's codes lie under chunks 2-3, so every thread holds its
+    // codes before any is rewritten.
+    //   bf16 query: QK^T needs f16 K as well, so the 32 k_pe codes (32B-swizzled
+    //     at stage + 32 KB, under the f16 k_pe tile) are widened too, half a
+    //     token row per thread.  V rows past L are zeroed by the softmax warps.
+    //   FP8 query: QK^T reads the codes themselves, so box 1's warps wait for
+    //     QK of the page before writing chunks 2-3, and the converter writes
+    //     zeros for tokens at or past L and for a page that was never loaded.
     const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
     const int t = ct & 63, h = ct >> 6;
+    const int tp = ct >> 1, hp = ct & 1;           // bf16 query: k_pe token and 16-code half
     int page_next = n_pages > 0 ? bt_row[0] : 0;
     for (int j = 0; j < n_pages; ++j) {
       const int st = j % kNS;
-      const int page = page_next;
-      if (j + 1 < n_pages) page_next = bt_row[j + 1];
-      const bool page_ok = page >= 0 && page < p.num_pages;
-      const bool zero = t >= (page_ok ? min(L - (lo + j * kPage), kPage) : 0);
+      bool zero = false;
+      if constexpr (kQ8) {
+        const int page = page_next;
+        if (j + 1 < n_pages) page_next = bt_row[j + 1];
+        const bool page_ok = page >= 0 && page < p.num_pages;
+        zero = t >= (page_ok ? min(L - (lo + j * kPage), kPage) : 0);
+      }
       if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[st], (j / kNS) & 1, p, 9))) break;
       uint8_t* stage = sKV + st * kStageBytes;
-      uint4 raw[8];
+      uint4 raw[8], rpe;
       const uint8_t* src = stage + kQ8RawOff + h * kQ8Box + t * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u) raw[u] = *reinterpret_cast<const uint4*>(src + ((u ^ (t & 7)) << 4));
-      conv_sync();  // every thread holds its codes before box 1's space is rewritten
-      const bool ok = h == 0 || __all_sync(0xffffffffu, wait_bar(ctl, &ctl->qk_done[st], (j / kNS) & 1, p, 25));
-      // Logical 16-code piece u of the row: bf16 chunk 2h + u/4, 16-byte units
+      if constexpr (!kQ8)  // 32B swizzle: the 16-byte unit flips with bit 2 of the row
+        rpe = *reinterpret_cast<const uint4*>(stage + kQ8RawPeOff + tp * 32 + ((hp ^ ((tp >> 2) & 1)) << 4));
+      bool ok = true;
+      if constexpr (kQ8) {
+        conv_sync();  // every thread holds its codes before box 1's space is rewritten
+        ok = h == 0 || __all_sync(0xffffffffu, wait_bar(ctl, &ctl->qk_done[st], (j / kNS) & 1, p, 25));
+      } else {
+        conv_sync();  // every thread holds its codes (c_kv and k_pe) before any is rewritten
+      }
+      // Logical 16-code piece u of the row: f16 chunk 2h + u/4, 16-byte units
       // 2(u%4) and 2(u%4)+1 of token row t (128B swizzle).
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -638,76 +695,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         uint32_t o[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          o[2 * q] = zero ? 0u : e4m3x2_to_bf16x2((uint16_t)(w[q] & 0xFFFFu));
-          o[2 * q + 1] = zero ? 0u : e4m3x2_to_bf16x2((uint16_t)(w[q] >> 16));
+          o[2 * q] = zero ? 0u : e4m3x2_to_f16x2((uint16_t)(w[q] & 0xFFFFu));
+          o[2 * q + 1] = zero ? 0u : e4m3x2_to_f16x2((uint16_t)(w[q] >> 16));
         }
         const int c0 = 2 * (u & 3);
         *reinterpret_cast<uint4*>(dst + ((c0 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ (t & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
-      if (conv_sync_or(!ok)) break;
+      if constexpr (!kQ8) {  // k_pe: 16 codes -> units 2hp, 2hp+1 of the 64B-swizzled f16 row tp
+        uint8_t* dst = stage + 4 * kKvChunkBytes + tp * 64;
+        const uint32_t w[4] = {rpe.x, rpe.y, rpe.z, rpe.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          o[2 * q] = e4m3x2_to_f16x2((uint16_t)(w[q] & 0xFFFFu));
+          o[2 * q + 1] = e4m3x2_to_f16x2((uint16_t)(w[q] >> 16));
+        }
+        *reinterpret_cast<uint4*>(dst + (((2 * hp) ^ ((tp >> 1) & 3)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(dst + (((2 * hp + 1) ^ ((tp >> 1) & 3)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      if constexpr (kQ8) {
+        if (conv_sync_or(!ok)) break;
+      }
       fence_proxy_async_smem();
       conv_sync();
       if (lane == 0) mbar_arrive(&ctl->full[st]);
-    }
-  } else if (kFp8 && !kQ8 && warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
-    // ------------------------------------------------------------ e4m3 -> bf16 converter
-    // Thread ct converts tokens ct/2 of chunks 2(ct%2) and 2(ct%2)+1 (64 e4m3
-    // bytes each, into 128-byte swizzled bf16 rows), and threads below 64 also
-    // token ct's 32 k_pe bytes (into 64-byte swizzled rows).
-    const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
-    const int t_c = ct >> 1, c0 = 2 * (ct & 1);
-    for (int j = 0; j < n_pages; ++j) {
-      const int s = j % kNS;
-      if (conv_sync_or(!wait_bar(ctl, &ctl->raw_full[s], (j / kNS) & 1, p, 9))) break;
-      uint8_t* stage = sKV + s * kStageBytes;
-      uint4 raw[2][4], rpe[2];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const uint4* src = reinterpret_cast<const uint4*>(stage + Lay::kRawOff + (c0 + k) * kRawBox + t_c * 64);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) raw[k][q] = src[q];
-      }
-      if (ct < 64) {
-        const uint4* src = reinterpret_cast<const uint4*>(stage + Lay::kRawPeOff + ct * 32);
-        rpe[0] = src[0];
-        rpe[1] = src[1];
-      }
-      conv_sync();  // every raw byte is in registers before the bf16 writes overlap them
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        uint8_t* dst = stage + (c0 + k) * kKvChunkBytes + t_c * 128;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t w[4] = {raw[k][q].x, raw[k][q].y, raw[k][q].z, raw[k][q].w};
-          uint32_t o[8];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            o[2 * h] = e4m3x2_to_bf16x2((uint16_t)(w[h] & 0xFFFFu));
-            o[2 * h + 1] = e4m3x2_to_bf16x2((uint16_t)(w[h] >> 16));
-          }
-          *reinterpret_cast<uint4*>(dst + (((2 * q) ^ (t_c & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ (t_c & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-      }
-      if (ct < 64) {
-        uint8_t* dst = stage + 4 * kKvChunkBytes + ct * 64;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint32_t w[4] = {rpe[q].x, rpe[q].y, rpe[q].z, rpe[q].w};
-          uint32_t o[8];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            o[2 * h] = e4m3x2_to_bf16x2((uint16_t)(w[h] & 0xFFFFu));
-            o[2 * h + 1] = e4m3x2_to_bf16x2((uint16_t)(w[h] >> 16));
-          }
-          *reinterpret_cast<uint4*>(dst + (((2 * q) ^ ((ct >> 1) & 3)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ ((ct >> 1) & 3)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-      }
-      fence_proxy_async_smem();
-      conv_sync();
-      if (lane == 0) mbar_arrive(&ctl->full[s]);
     }
   } else if (warp >= send_warp0<kFp8>() && warp < send_warp0<kFp8>() + 4) {
     // ------------------------------------------------------------ S sender
@@ -788,6 +800,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     float l_sum = 0.f;         // exp sum over this CTA's token halves, relative to r_ref
     int own_fixes = 0;         // pages on which this warp scaled its own P rows (p_recv phases)
     bool poisoned = !len_ok;
+    bool q_bad = false;        // this row's query does not fit the FP8-cache path's f16 operands
     bool ok = true;
 
     // 16-byte chunk u (tokens 8u..8u+7) of this thread's row of P.  P is K-major
@@ -866,9 +879,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
             uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[i]));
-              __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
-              wv[i] = *reinterpret_cast<uint32_t*>(&y);
+              wv[i] = scale_pair<kFp8>(wv[i], f);
             }
             *c = w;
           }
@@ -902,7 +913,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
         ok = false;
       } else {
         // bf16: four 64-column chunks (2 per TMEM column); FP8: two 128-code
-        // chunks (4 per column).  Either way a chunk row is 128 bytes.
+        // chunks (4 per column).  Either way a chunk row is 128 bytes.  With an
+        // FP8 cache and a bf16 query the values become f16 on the way (the
+        // MMAs' operand type there), and so do the row's q_pe values in place.
+        bool big = false;
         for (int k = 0; k < (kQ8 ? 2 : 4); ++k) {
           const uint8_t* qrow = sQ + k * kQChunkBytes + r * 128;
           uint32_t w[2][16];
@@ -914,8 +928,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
             w[u >> 2][(u & 3) * 4 + 2] = v.z;
             w[u >> 2][(u & 3) * 4 + 3] = v.w;
           }
+          if constexpr (kFp8 && !kQ8) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i >> 4][i & 15] = bf16x2_to_f16x2(w[i >> 4][i & 15], big);
+          }
           tmem_st16(tmem + lane_base + kColQ + k * 32, w[0]);
           tmem_st16(tmem + lane_base + kColQ + k * 32 + 16, w[1]);
+        }
+        if constexpr (kFp8 && !kQ8) {  // the row's 32 q_pe values: 64 bytes (swizzle stays inside the row)
+          uint4* qp = reinterpret_cast<uint4*>(sQpe + r * 64);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 v = qp[u];
+            v.x = bf16x2_to_f16x2(v.x, big);
+            v.y = bf16x2_to_f16x2(v.y, big);
+            v.z = bf16x2_to_f16x2(v.z, big);
+            v.w = bf16x2_to_f16x2(v.w, big);
+            qp[u] = v;
+          }
+          fence_proxy_async_smem();  // the f16 q_pe is what the QK issuer's MMAs read
+          if (big && row_ok) {  // index -4: a query value outside the f16 range of this path
+            q_bad = true;
+            report_error(p.err, MLA_ERR_DEVICE_INPUT, b, -4, row0 + r);
+          }
         }
         tmem_st_wait();
       }
@@ -1031,8 +1066,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
             const float p0 = ex2(fmaf(sv[u * 8 + 2 * h], sc2, nm));
             const float p1 = ex2(fmaf(sv[u * 8 + 2 * h + 1], sc2, nm));
             part[h] += p0 + p1;
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-            w[h] = *reinterpret_cast<uint32_t*>(&b2);
+            w[h] = pack_pair<kFp8>(p0, p1);
           }
           pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
         }
@@ -1046,8 +1080,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
             const float p0 = (x0 == -INFINITY) ? 0.f : ex2(x0 - r_ref);
             const float p1 = (x1 == -INFINITY) ? 0.f : ex2(x1 - r_ref);
             part[h] += p0 + p1;
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-            w[h] = *reinterpret_cast<uint32_t*>(&b2);
+            w[h] = pack_pair<kFp8>(p0, p1);
           }
           pk[u] = make_uint4(w[0], w[1], w[2], w[3]);
         }
@@ -1088,7 +1121,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
 
     // ------------------------------------------------------------ epilogue
     // Row sums of both token halves: every row's partial goes to the peer.
-    st_async_u32(mapa_shared(smem_u32(&ctl->l_peer[r]), peer), __float_as_uint(l_sum),
+    // (NaN marks a row whose query this CTA found out of range: the peer writes
+    // it as NaN too.)
+    st_async_u32(mapa_shared(smem_u32(&ctl->l_peer[r]), peer), __float_as_uint(q_bad ? NAN : l_sum),
                  mapa_shared(smem_u32(&ctl->fin), peer));
     if (lane == 0) mbar_arrive_expect_tx(&ctl->fin, 32 * 4);
     if (poisoned) atomicOr(&ctl->poisoned, 1);
@@ -1098,7 +1133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     tc_fence_after();
     __syncwarp();
     const bool have_o = !fail && n_pages > 0;
-    const bool bad = ctl->poisoned != 0 || fail;
+    const bool bad = ctl->poisoned != 0 || fail || (kFp8 && !kQ8 && (q_bad || ctl->l_peer[r] != ctl->l_peer[r]));
     const float l_tot = l_sum + ctl->l_peer[r];
     const bool has = l_tot > 0.f;
     const float il = has ? kv_scale / l_tot : 0.f;
@@ -1308,15 +1343,16 @@ cudaError_t launch_split_kv(const DecodeParams& p, cudaStream_t stream) {
                  CU_TENSOR_MAP_SWIZZLE_64B, 32))
     return cudaErrorInvalidValue;
   const bool ok = p.kv_fp8 ? encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64,
-                                       CU_TENSOR_MAP_SWIZZLE_NONE)
+                                       CU_TENSOR_MAP_SWIZZLE_128B, 128)
                            : encode_2d(&tm_kv, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
                                        CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   // bf16 cache viewed as [chunk 0..8][row][64 columns]: row stride 1152 B, chunk stride 128 B.
   if (!p.kv_fp8 && !encode_kv_chunks(&tm_kv3, p.kv, kv_rows)) return cudaErrorInvalidValue;
-  // 32 k_pe columns per box: bf16 with 64-byte swizzled rows, or 32 e4m3 bytes.
+  // 32 k_pe columns per box: bf16 with 64-byte swizzled rows, or 32 e4m3 bytes
+  // with 32-byte swizzled rows.
   if (!(p.kv_fp8 ? encode_2d(&tm_kpe, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 64,
-                             CU_TENSOR_MAP_SWIZZLE_NONE, 32)
+                             CU_TENSOR_MAP_SWIZZLE_32B, 32)
                  : encode_2d(&tm_kpe, p.kv, kRow, kv_rows, kRow, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
                              CU_TENSOR_MAP_SWIZZLE_64B, 32)))
     return cudaErrorInvalidValue;

@@ -310,6 +310,33 @@ def test_device_input_errors_are_reported_and_isolated():
     assert _lib.check_error(ws)[0] == _lib.MLA_ERR_DEVICE_INPUT
 
 
+@pytest.mark.parametrize("splits", [1, 2])
+def test_fp8_cache_query_beyond_f16_range_is_reported(splits):
+    # With an FP8 cache the MMAs take f16 operands, so a bf16 query must lie
+    # within +-65504: a value beyond it is a device-side input error (index -4,
+    # value = the row within the request) whose row alone comes out as NaN.
+    inp = small(950, 2, [2, 100, 300], H=16, kv_fp8=True)
+    ref_o, ref_l = oracle.decode(inp)
+    dev = inp.to("cuda")
+    row = 1 * 16 + 3                      # query token 1, head 3 of request 2 (two splits when s=2)
+    q_nope = dev.q_nope.clone()
+    q_nope[2, 1, 3, 77] = 131072.0        # 2^17, exact in bf16
+    bad = synth.Inputs(**{**dev.__dict__})
+    bad.q_nope = q_nope
+    pl = api.plan_for(dev, force_splits=splits)
+    ws = api.alloc_workspace(pl, "cuda")
+    out, lse, _ = api.decode(bad, pl=pl, workspace=ws, check=False, out_fp32=True)
+    st, info = _lib.check_error(ws)
+    assert st == _lib.MLA_ERR_DEVICE_INPUT and list(info[1:]) == [2, -4, row]
+    assert torch.isnan(out[2, 1, 3]).all() and torch.isnan(lse[2, 1, 3])
+    out[2, 1, 3] = torch.from_numpy(ref_o[2, 1, 3]).float().cuda()
+    lse[2, 1, 3] = float(ref_l[2, 1, 3])
+    compare(out, lse, ref_o, ref_l, fp8=True, what=f"every other row, s={splits}")
+    # the unmodified query runs clean on the same workspace
+    api.decode(dev, pl=pl, workspace=ws, check=False)
+    assert _lib.check_error(ws)[0] == _lib.MLA_OK
+
+
 # ---------------------------------------------------------------------------
 # Full-size workloads, in the launch configuration the benchmark times (the
 # planner's split count), with EVERY request checked against the oracle (the
