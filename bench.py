@@ -3,7 +3,9 @@
 One step = one full decode call (split-KV attention kernel + LSE combine) over
 the resident synthetic MTP-3 workload (B=64, H=32, q_len=4, kv_len=81920,
 page 64, bf16 cache).  The KV stream (6.04 GB) is larger than L2, so no flush
-is needed between timed steps.  Prints one JSON line.
+is needed between timed steps; workloads that read less than four times the L2
+size (plain, tiny) get L2 flushed by a 2x-L2 write before every timed step and
+are timed per step with events (``--l2-flush``).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -241,6 +243,8 @@ def main():
                     help="override the request count (smaller cases of the same kernel for ncu)")
     ap.add_argument("--force-splits", type=int, default=0, help="override the planner's split count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2-flush", default="auto", choices=["auto", "on", "off"],
+                    help="write a 2x-L2 buffer before every timed step (auto: when a call reads < 4x L2)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -290,6 +294,16 @@ def main():
     def step(ev=None):
         call(qn, qp, inp.block_table, inp.seq_lens, ev)
 
+    # L2 hygiene: a call that reads less than four times the L2 size would find
+    # part of its inputs left in L2 by the previous step, so such workloads get
+    # a 2x-L2 write before each timed step and are timed per step with events
+    # (the flush is outside the bracket); larger ones stream past L2.
+    l2_bytes = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    out_b = 4 if inp.out_fp32 else 2
+    abytes = algorithmic_bytes(inp, out_b)
+    flush = args.l2_flush == "on" or (args.l2_flush == "auto" and abytes < 4 * l2_bytes)
+    scrub = torch.empty(2 * l2_bytes // 4, dtype=torch.int32, device="cuda") if flush else None
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -306,6 +320,8 @@ def main():
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(args.steps):
+        if flush:
+            scrub.fill_(k)
         step(evs[k])
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -314,7 +330,10 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     split_ms = [e[0].elapsed_time(e[1]) for e in evs]
     comb_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    step_us = total_ms / args.steps * 1e3
+    if flush:  # per-step brackets: the flush writes between them are not the decode's
+        step_us = statistics.mean(e[0].elapsed_time(e[2]) for e in evs) * 1e3
+    else:
+        step_us = total_ms / args.steps * 1e3
     step_us = max_over_ranks(world, step_us)
     split_us = statistics.mean(split_ms) * 1e3
     comb_us = statistics.mean(comb_ms) * 1e3
@@ -417,8 +436,6 @@ def main():
     assert st == 0, (st, info)
 
     hbm_peak, tc_peak, tc_sus, peak_kind = read_peaks()
-    out_b = 4 if inp.out_fp32 else 2
-    abytes = algorithmic_bytes(inp, out_b)
     aflops = algorithmic_flops(inp)
     achieved_gbs = abytes / (split_us * 1e-6) / 1e9
     achieved_tf = aflops / (split_us * 1e-6) / 1e12
@@ -458,7 +475,8 @@ def main():
                                f"{', e4m3 Q' if q8 else ''}",
                    "num_kv_splits": pl.num_kv_splits, "chunk_tokens": pl.chunk_tokens,
                    "row_groups": pl.row_groups, "partial_bytes": pl.partial_bytes,
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+                   "l2": ("L2 flushed before every timed step (2x-L2 write), per-step events" if flush
+                          else "inputs larger than L2 (no flush)"), "parallelism": f"replicas x{world}"},
         "gb_per_s": abytes * world / (step_us * 1e-6) / 1e9,
         "tflops": aflops * world / (step_us * 1e-6) / 1e12,
         "kernel_us": ({"split_kv+combine": split_us} if q8 else {"split_kv": split_us, "combine": comb_us}),
