@@ -220,8 +220,8 @@ mla_status_t mla_decode_varlen(const mla_decode_plan_t* plan, const void* q_nope
  * names the follow-up "pass output_scale and assert FP8 Q").  QK^T runs on
  * the e4m3 codes of query and cache on the FP8 tensor path (products of e4m3
  * codes are exact, so the scores equal those on the dequantised values up to
- * fp32 summation order); P and V stay bf16 for PV, V being the cache codes
- * widened exactly.
+ * fp32 summation order); P and V stay 16-bit (f16) for PV, V being the cache
+ * codes widened exactly.
  *
  * Same arguments as mla_decode, except:
  *   plan    : kv_dtype must be MLA_KV_FP8_E4M3 (else MLA_ERR_UNSUPPORTED)

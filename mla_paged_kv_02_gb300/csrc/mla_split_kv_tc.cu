@@ -26,8 +26,8 @@
 //   warp 0     TMA producer: Q once, then per page a block-table lookup and the
 //              CTA's columns of the page into a 4-stage ring (bf16: one 3-D box
 //              of four 64x64 chunks, 128B swizzle, and one 32-column k_pe box,
-//              64B swizzle; FP8: four boxes of 64x64 e4m3 bytes and one of
-//              32x64); owns the TMEM allocation.
+//              64B swizzle; FP8: two 128B-swizzled boxes of 128 e4m3 codes and
+//              one 32B-swizzled box of 32); owns the TMEM allocation.
 //   warp 1     QK^T issuer (one thread).
 //   warps 2-5  softmax / exchange / epilogue warpgroup.  Warp w reads TMEM lane
 //              quadrant w%4 (rows 32*(w%4) .. +31) and works on its CTA's token
@@ -37,11 +37,11 @@
 //   warps 6-9  (bf16 cache; 10-13 with an FP8 cache) S senders: the peer's
 //              token half of S(j) from TMEM to the peer, off the softmax warps'
 //              chain.
-//   warps 6-9  (FP8 cache) converter: the CTA's e4m3 columns land in the upper
-//              half of a stage; every thread first pulls its share into
-//              registers, then writes exact bf16 values (e4m3 is a subset of
-//              bf16) in the swizzled layout.  The per-tensor scale is folded into
-//              the softmax scale and the epilogue.
+//   warps 6-9  (FP8 cache) converter: the CTA's e4m3 columns land at stage +
+//              16 KB; each thread pulls one token row of codes into registers,
+//              then writes exact f16 values (every e4m3 value is an f16) in the
+//              swizzled layout.  The per-tensor scale is folded into the softmax
+//              scale and the epilogue.
 //   warp 10    PV issuer (one thread; warp 14 with an FP8 cache).
 //
 // Q's c_kv columns are kept in tensor memory as the A operand of QK^T (read every
@@ -537,7 +537,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(block_threads<kFp8>(
     if constexpr (kQ8) {
      if (lane == 0 && n_pages > 0) {
       // FP8 query: QK(j) on the page's e4m3 codes as soon as they land (the
-      // converter's bf16 V is only needed by PV): 8 K-steps of 32 codes over the
+      // converter's f16 V is only needed by PV): 8 K-steps of 32 codes over the
       // two c_kv boxes, A from tensor memory, and one over the 32 k_pe codes, A
       // (q_pe) from shared memory.  qk_done tells the converter that the codes
       // under V chunks 2 and 3 may be overwritten.
