@@ -59,6 +59,12 @@ def algorithmic_flops(inp):
     return 2176 * visible_pairs(inp)
 
 
+def needs_l2_flush(call_bytes, l2_bytes, mode="auto"):
+    """Flush L2 before every timed step?  'auto': when a call reads less than four
+    times the L2 size (its inputs would partly survive in L2 between steps)."""
+    return mode == "on" or (mode == "auto" and call_bytes < 4 * l2_bytes)
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -301,7 +307,7 @@ def main():
     l2_bytes = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
     out_b = 4 if inp.out_fp32 else 2
     abytes = algorithmic_bytes(inp, out_b)
-    flush = args.l2_flush == "on" or (args.l2_flush == "auto" and abytes < 4 * l2_bytes)
+    flush = needs_l2_flush(abytes, l2_bytes, args.l2_flush)
     scrub = torch.empty(2 * l2_bytes // 4, dtype=torch.int32, device="cuda") if flush else None
 
     for _ in range(args.warmup):
