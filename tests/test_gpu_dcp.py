@@ -193,3 +193,39 @@ def test_bad_shard_range_is_reported_and_isolated():
     assert torch.isnan(part[1]).all()
     ref = oracle.decode_range(inp, lo, hi)
     check_partial(part[[0, 2]], ref[[0, 2]], False, "valid requests")
+
+
+def test_dcp_decode_through_nccl_on_one_rank():
+    # dcp.decode end to end with a real NCCL process group.  One GPU gives one
+    # rank (ranks on one GPU would wait on one another's kernels), so the
+    # all-gather is NCCL's with a world of one: the shard is the whole sequence
+    # and the merged result must equal the oracle's and mla_decode's.
+    import torch.distributed as dist
+
+    if not dist.is_nccl_available():
+        pytest.skip("torch built without NCCL")
+    inp = synth.make_inputs("tiny", seed=80, kv_lens=[3, 70, 200, 641], q_len=2, batch=4, num_heads=32, sharp=4.0)
+    ref_o, ref_l = oracle.decode(inp)
+    dev = inp.to("cuda")
+    store = dist.HashStore()
+    dist.init_process_group("nccl", store=store, rank=0, world_size=1)
+    try:
+        bounds = dcp.shard_bounds(dev.seq_lens.tolist(), 1, 0)
+        bt = dcp.local_block_table(dev.block_table, bounds)
+        sl = torch.tensor([e - s for s, e in bounds], dtype=torch.int32, device="cuda")
+        ss = torch.tensor([s for s, _ in bounds], dtype=torch.int32, device="cuda")
+        pl = _lib.plan(dev.batch, dev.num_heads, dev.q_len, max(int(sl.max()), dev.q_len), force_splits=0)
+        ws = api.alloc_workspace(pl, "cuda")
+        out = torch.empty((dev.batch, dev.q_len, dev.num_heads, 512), dtype=torch.float32, device="cuda")
+        lse = torch.empty((dev.batch, dev.q_len, dev.num_heads), dtype=torch.float32, device="cuda")
+        parts = dcp.decode(pl, dev.q_nope, dev.q_pe, dev.kv_cache, bt, sl, ss, dev.seq_lens, dev.softmax_scale,
+                           api.kv_scale_tensor(dev), out, lse, ws, group=dist.group.WORLD)
+        torch.cuda.synchronize()
+        assert parts.shape == (1, dev.batch, dev.q_len, dev.num_heads, 513)
+        assert _lib.check_error(ws)[0] == _lib.MLA_OK
+    finally:
+        dist.destroy_process_group()
+    check_out(out, lse, ref_o, ref_l, False, "DCP through NCCL, world 1")
+    o2, l2, _ = api.decode(dev, out_fp32=True)
+    torch.cuda.synchronize()
+    assert torch.allclose(out, o2, rtol=0, atol=1e-5) and torch.allclose(lse, l2, rtol=0, atol=1e-5)
