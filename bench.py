@@ -390,12 +390,14 @@ def main():
     torch.cuda.synchronize()
     e2e_serial_us = max_over_ranks(world, e0.elapsed_time(e1) / args.steps * 1e3)
 
-    # Pipelined, as a serving loop runs: the same copies, every step, but on a
-    # copy stream with two sets of device buffers, so that step k+1's inputs
-    # go in and step k's result comes out while step k decodes.  Step k waits
-    # for its own inputs; a buffer set is reused only once its previous decode
-    # and read-back have finished.
-    copy_stream = torch.cuda.Stream()
+    # Pipelined, as a serving loop runs: the same copies, every step, but on
+    # two copy streams (host to device, device to host: both directions move at
+    # once) with two sets of device buffers, so that step k+1's inputs go in
+    # and step k's result comes out while step k decodes.  Step k waits for its
+    # own inputs; a buffer set is reused only once its previous decode and
+    # read-back have finished.
+    copy_stream = torch.cuda.Stream()   # host to device
+    back_stream = torch.cuda.Stream()   # device to host
     sets = [dict(qn=torch.empty_like(qn), qp=torch.empty_like(qp), bt=torch.empty_like(inp.block_table),
                  sl=torch.empty_like(inp.seq_lens), out=torch.empty_like(out), lse=torch.empty_like(lse),
                  h_out=torch.empty(out.shape, dtype=out.dtype).pin_memory(),
@@ -419,11 +421,11 @@ def main():
             stream.wait_event(b["d2h"])  # its previous result has been read back
             decode_into(b["qn"], b["qp"], b["bt"], b["sl"], b["out"], b["lse"])
             b["done"].record(stream)
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(b["done"])
+            with torch.cuda.stream(back_stream):
+                back_stream.wait_event(b["done"])
                 b["h_out"].copy_(b["out"], non_blocking=True)
                 b["h_lse"].copy_(b["lse"], non_blocking=True)
-                b["d2h"].record(copy_stream)
+                b["d2h"].record(back_stream)
 
     run_pipelined(args.warmup)
     torch.cuda.synchronize()
@@ -433,6 +435,7 @@ def main():
     p0.record(copy_stream)
     run_pipelined(args.steps)
     stream.wait_stream(copy_stream)
+    stream.wait_stream(back_stream)
     p1.record(stream)
     torch.cuda.synchronize()
     e2e_us = max_over_ranks(world, p0.elapsed_time(p1) / args.steps * 1e3)
@@ -492,7 +495,7 @@ def main():
         # the cross-stream waits cost more than they hide); both are reported.
         "e2e": {"value": min(e2e_us, e2e_serial_us), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "mode": ("copies on a second stream, overlapping the neighbouring steps' decodes"
+                "mode": ("copies on two copy streams (one per direction), overlapping the neighbouring steps' decodes"
                          if e2e_us <= e2e_serial_us else "one stream: copy in, decode, copy out"),
                 "pipelined_value": e2e_us, "serial_value": e2e_serial_us},
         "gpu_launches": args.steps * (1 + (pl.num_kv_splits > 1)),
