@@ -310,6 +310,19 @@ def test_device_input_errors_are_reported_and_isolated():
     assert _lib.check_error(ws)[0] == _lib.MLA_ERR_DEVICE_INPUT
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_one_long_request_at_the_planners_split_count(fp8):
+    # A single 128k-token request with 128 query rows (one cluster per split):
+    # the planner spreads it over many splits, and past 32 splits the combine
+    # takes its general path.  Every row against the oracle.
+    inp = synth.make_inputs("tiny", seed=1700 + fp8, kv_lens=[131072 - 5], q_len=2, batch=1, num_heads=64,
+                            sharp=3.0, kv_fp8=fp8)
+    ref_o, ref_l = oracle.decode(inp)
+    out, lse, pl = run(inp, out_fp32=True)
+    assert pl.num_kv_splits > 32
+    compare(out, lse, ref_o, ref_l, fp8=fp8, what=f"one 128k request s={pl.num_kv_splits}")
+
+
 @pytest.mark.parametrize("splits", [1, 2])
 def test_fp8_cache_query_beyond_f16_range_is_reported(splits):
     # With an FP8 cache the MMAs take f16 operands, so a bf16 query must lie
