@@ -310,6 +310,18 @@ def test_device_input_errors_are_reported_and_isolated():
     assert _lib.check_error(ws)[0] == _lib.MLA_ERR_DEVICE_INPUT
 
 
+@pytest.mark.parametrize("q_len,H", [(8, 128), (8, 512)])
+def test_many_row_groups(q_len, H):
+    # 1024 and 4096 query rows per request (8 and 32 row groups of 128, the
+    # latter the planner's maximum): every group's cluster against the oracle.
+    inp = small(1800 + H, q_len, [q_len, 100, 700], H=H, sharp=3.0)
+    ref_o, ref_l = oracle.decode(inp)
+    for s in (0, 3):
+        out, lse, pl = run(inp, force_splits=s, out_fp32=True)
+        assert pl.row_groups == q_len * H // 128
+        compare(out, lse, ref_o, ref_l, what=f"{q_len * H} rows s={pl.num_kv_splits}")
+
+
 @pytest.mark.parametrize("fp8", [False, True])
 def test_one_long_request_at_the_planners_split_count(fp8):
     # A single 128k-token request with 128 query rows (one cluster per split):
