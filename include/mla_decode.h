@@ -103,6 +103,33 @@ mla_status_t mla_decode_plan(int batch, int num_heads, int q_len, int max_seq_le
                              mla_decode_plan_t* plan);
 
 /*
+ * mla_decode_plan_lengths -- the same plan, with the split count chosen from
+ * the batch's own lengths rather than from an upper bound (a balanced split
+ * scheduler for uneven lengths, the TokenSpeed MLA summary's scheduler item).
+ * Host-only.
+ *
+ *   seq_lens : host int32 [batch], the lengths the call will see (q_len <= L_b)
+ *   other arguments as mla_decode_plan (max_seq_len = the largest seq_lens[b])
+ *
+ * Every candidate split count up to the length-blind plan's for the longest
+ * request is tried on a model of the split kernel: each (request, split, row
+ * group) cluster costs a fixed 13 page-times plus its pages (1 for a split
+ * past its request's end), clusters start in the kernel's order (requests
+ * longest first when it ranks them) on the first cluster slot to free, and
+ * partial traffic plus the combine's fixed cost are added when a request has
+ * more than one split; the smallest modelled time wins (ties to fewer
+ * splits).  With equal lengths this is the length-blind choice or one with
+ * fewer waves; with uneven lengths the long requests dominate and fewer
+ * splits win.  O(splits x batch x row groups x log SMs) host work.  The plan
+ * serves only calls whose lengths are at most the ones given; errors as
+ * mla_decode_plan, plus MLA_ERR_INVALID_ARG for a NULL seq_lens or an
+ * L_b < q_len.
+ */
+mla_status_t mla_decode_plan_lengths(int batch, int num_heads, int q_len, const int32_t* seq_lens,
+                                     int page_size, mla_kv_dtype_t kv_dtype, int num_sms,
+                                     mla_decode_plan_t* plan);
+
+/*
  * mla_workspace_init -- zero the workspace header (the sticky device error
  * word) once after the caller allocates the workspace.  Asynchronous on stream.
  * Library plumbing with no counterpart on the source pages: it exists because

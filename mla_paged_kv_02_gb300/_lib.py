@@ -32,6 +32,7 @@ MLA_OUT_FP8_E4M3 = 2
 # Every symbol include/mla_decode.h declares.
 EXPORTED = (
     "mla_decode_plan",
+    "mla_decode_plan_lengths",
     "mla_workspace_init",
     "mla_decode",
     "mla_split_kv",
@@ -107,6 +108,7 @@ def _open(path: str) -> ctypes.CDLL:
     P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     PP = ctypes.POINTER(Plan)
     lib.mla_decode_plan.argtypes = [I, I, I, I, I, I, I, I, PP]
+    lib.mla_decode_plan_lengths.argtypes = [I, I, I, P, I, I, I, PP]
     lib.mla_workspace_init.argtypes = [P, SZ, P]
     decode_args = [PP, P, I64, P, I64, P, I, P, I, P, F, P, P, I, P, P, SZ, P]
     lib.mla_decode.argtypes = decode_args
@@ -138,6 +140,20 @@ def plan(batch: int, num_heads: int, q_len: int, max_seq_len: int, kv_fp8: bool 
                                 ctypes.byref(p))
     if st != MLA_OK:
         raise MlaError(st, "mla_decode_plan")
+    return p
+
+
+def plan_lengths(num_heads: int, q_len: int, seq_lens, kv_fp8: bool = False, num_sms: int = 0,
+                 page_size: int = 64) -> Plan:
+    """mla_decode_plan_lengths: the split count from the batch's own lengths
+    (any int sequence or tensor; copied to host int32)."""
+    lens = torch.as_tensor(seq_lens).to(device="cpu", dtype=torch.int32).contiguous()
+    p = Plan()
+    st = load().mla_decode_plan_lengths(int(lens.numel()), num_heads, q_len, ctypes.c_void_p(lens.data_ptr()),
+                                        page_size, MLA_KV_FP8_E4M3 if kv_fp8 else MLA_KV_BF16, num_sms,
+                                        ctypes.byref(p))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_decode_plan_lengths")
     return p
 
 

@@ -12,6 +12,10 @@ from . import _lib
 
 
 def plan_for(inp, force_splits: int = 0, num_sms: int = 0, max_seq_len: Optional[int] = None) -> _lib.Plan:
+    """The plan for ``inp``: from its own lengths (mla_decode_plan_lengths) unless
+    a split count is forced or the plan must cover longer calls (max_seq_len)."""
+    if force_splits == 0 and max_seq_len is None:
+        return _lib.plan_lengths(inp.num_heads, inp.q_len, inp.seq_lens, kv_fp8=inp.kv_fp8, num_sms=num_sms)
     return _lib.plan(inp.batch, inp.num_heads, inp.q_len,
                      max_seq_len if max_seq_len is not None else inp.max_seq_len,
                      kv_fp8=inp.kv_fp8, num_sms=num_sms, force_splits=force_splits)

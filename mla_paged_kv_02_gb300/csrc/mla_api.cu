@@ -3,6 +3,12 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
+#include <functional>
+#include <numeric>
+#include <queue>
+#include <vector>
+
 #include "common.cuh"
 #include "kernels.h"
 #ifdef MLA_DEBUG
@@ -31,6 +37,13 @@ constexpr int kMaxRows = 4096;  // num_heads * q_len per request
 constexpr int kMaxSeqLen = 1 << 30;
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Length-aware planning (mla_decode_plan_lengths): costs in page-times of one
+// cluster, measured on the split kernel.  A cluster's fixed cost (set-up, the
+// drain after its last load, the epilogue) is about 14 us against about 1.1 us
+// per page; a cluster whose split lies past its request's end exits at once.
+constexpr double kClusterPages = 13.0;
+constexpr double kEmptyClusterPages = 1.0;
 
 // Bytes of fp32 split partials [batch, q_len, H, splits, 513]; none with one split.
 size_t partial_bytes_for(int64_t batch, int64_t rows, int64_t splits) {
@@ -231,6 +244,74 @@ mla_status_t mla_split_kv(const mla_decode_plan_t* plan, const void* q_nope, int
   if (st != MLA_OK) return st;
   if (launch_split_kv(p, (cudaStream_t)cuda_stream) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
+}
+
+mla_status_t mla_decode_plan_lengths(int batch, int num_heads, int q_len, const int32_t* seq_lens,
+                                     int page_size, mla_kv_dtype_t kv_dtype, int num_sms,
+                                     mla_decode_plan_t* plan) {
+  if (!plan) return MLA_ERR_INVALID_ARG;
+  memset(plan, 0, sizeof *plan);
+  if (!seq_lens || batch < 1) return MLA_ERR_INVALID_ARG;
+  int max_len = q_len;
+  for (int b = 0; b < batch; ++b) {
+    if (seq_lens[b] < q_len) return MLA_ERR_INVALID_ARG;
+    max_len = std::max(max_len, (int)seq_lens[b]);
+  }
+  // The length-blind plan for the longest request: its split count bounds the
+  // candidates (uneven lengths only ever want fewer splits) and its checks
+  // apply unchanged.
+  mla_decode_plan_t uni;
+  mla_status_t st = mla_decode_plan(batch, num_heads, q_len, max_len, page_size, kv_dtype, num_sms, 0, &uni);
+  if (st != MLA_OK) return st;
+  const int64_t rows = (int64_t)num_heads * q_len;
+  const int rg = uni.row_groups;
+  const int slots = std::max(1, uni.num_sms / kCtasPerGroup);
+  const int pages = ceil_div(max_len, MLA_PAGE_SIZE);
+  const double page_bytes = (kv_dtype == MLA_KV_FP8_E4M3 ? 1.0 : 2.0) * MLA_KV_ROW * MLA_PAGE_SIZE;
+  std::vector<int> req_pages(batch), order(batch);
+  for (int b = 0; b < batch; ++b) req_pages[b] = ceil_div(seq_lens[b], MLA_PAGE_SIZE);
+  std::iota(order.begin(), order.end(), 0);
+  std::vector<int> by_len = order;  // the kernel's longest-first order (ties by index)
+  std::stable_sort(by_len.begin(), by_len.end(), [&](int a, int c) { return seq_lens[a] > seq_lens[c]; });
+
+  // Each candidate split count: the clusters in the order the hardware starts
+  // them (grid order, requests longest first when the kernel ranks them), each
+  // taken by the cluster slot that frees first; plus the combine's partial
+  // traffic and fixed cost when any request has more than one split.
+  int best_s = uni.num_kv_splits;
+  double best = 1e300;
+  for (int s = 1; s <= uni.num_kv_splits; ++s) {
+    const int chunk = ceil_div(pages, s);
+    if (ceil_div(pages, chunk) != s) continue;  // not a distinct plan
+    const bool lpt = batch <= kMaxOrderedBatch && (int64_t)batch * rg * s > slots;
+    const std::vector<int>& seq = lpt ? by_len : order;
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < slots; ++i) free_at.push(0.0);
+    double part_bytes = 0.0;
+    for (int b : seq) {
+      const int sb = std::max(1, std::min(s, ceil_div(req_pages[b], chunk)));
+      if (sb > 1) part_bytes += 2.0 * rows * sb * (MLA_KV_LORA_RANK + 1) * 4.0;
+      for (int k = 0; k < s; ++k) {
+        const double cost = k < sb ? kClusterPages + std::min(chunk, req_pages[b] - k * chunk) : kEmptyClusterPages;
+        for (int r = 0; r < rg; ++r) {
+          const double t = free_at.top();
+          free_at.pop();
+          free_at.push(t + cost);
+        }
+      }
+    }
+    double makespan = 0.0;
+    while (!free_at.empty()) {
+      makespan = std::max(makespan, free_at.top());
+      free_at.pop();
+    }
+    if (part_bytes > 0) makespan += part_bytes / (uni.num_sms * page_bytes) + kCombinePages;
+    if (makespan < best * (1.0 - 1e-9)) {
+      best = makespan;
+      best_s = s;
+    }
+  }
+  return mla_decode_plan(batch, num_heads, q_len, max_len, page_size, kv_dtype, uni.num_sms, best_s, plan);
 }
 
 }  // extern "C"

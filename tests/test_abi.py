@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from mla_paged_kv_02_gb300 import _lib
 
@@ -206,3 +207,30 @@ def test_fp8_entry_point_validation(lib):
     assert call(pl8, ps=72) == _lib.MLA_ERR_INVALID_ARG
     assert call(pl8, odt=7) == _lib.MLA_ERR_INVALID_ARG
     assert _call_decode(lib, plb, odt=_lib.MLA_OUT_FP8_E4M3) == _lib.MLA_ERR_INVALID_ARG
+
+
+def test_length_aware_plan():
+    # mla_decode_plan_lengths: host-only, never more splits than the length-blind
+    # plan for the longest request, the same geometry rules, and fewer splits when
+    # a few long requests dominate a batch of uneven lengths.
+    g = torch.Generator().manual_seed(3)
+    equal = [81920] * 64
+    p_len = _lib.plan_lengths(32, 4, equal, num_sms=152)
+    p_uni = _lib.plan(64, 32, 4, 81920, num_sms=152)
+    assert p_len.num_kv_splits == p_uni.num_kv_splits == 7  # the MTP-3 shape
+    assert p_len.workspace_bytes == p_uni.workspace_bytes
+    uneven = torch.randint(1, 131073, (256,), generator=g).tolist()
+    p_len = _lib.plan_lengths(16, 1, uneven, num_sms=152)
+    p_uni = _lib.plan(256, 16, 1, max(uneven), num_sms=152)
+    assert p_len.max_seq_len == max(uneven)
+    assert 1 <= p_len.num_kv_splits < p_uni.num_kv_splits
+    assert p_len.num_kv_splits * p_len.chunk_tokens >= max(uneven)
+    # a single request spreads over every cluster slot
+    one = _lib.plan_lengths(64, 2, [131072 - 5], num_sms=152)
+    assert one.num_kv_splits == _lib.plan(1, 64, 2, 131072 - 5, num_sms=152).num_kv_splits
+    for bad in ([3, 1], []):  # a length below q_len, an empty batch
+        with pytest.raises(_lib.MlaError):
+            _lib.plan_lengths(16, 2, bad, num_sms=152)
+    lib = _lib.load()
+    pl = _lib.Plan()
+    assert lib.mla_decode_plan_lengths(4, 16, 1, None, 64, 0, 152, ctypes.byref(pl)) == _lib.MLA_ERR_INVALID_ARG

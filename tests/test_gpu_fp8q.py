@@ -31,8 +31,8 @@ def built():
 
 
 def run_fp8(dev, splits=0, out_kind="fp32", out_scale=None, pl=None):
-    if pl is None:
-        pl = _lib.plan(dev.batch, dev.num_heads, dev.q_len, dev.max_seq_len, kv_fp8=True, force_splits=splits)
+    if pl is None:  # the benchmark's plan (from the batch's lengths) unless a split count is forced
+        pl = api.plan_for(dev, force_splits=splits)
     ws = api.alloc_workspace(pl, "cuda")
     shape = (dev.batch, dev.q_len, dev.num_heads, 512)
     dt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}[out_kind]
